@@ -1,0 +1,231 @@
+"""CPU oracle for the fine-grained FP8 GEMM path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module. The product path
+(the CUDA library ``libfp8bs.so`` and its Python binding) never does; the two
+share no code.
+
+What it computes, and the passage each step follows:
+
+* FP8 encoding and the two quantizers live in ``fp8bs_oracle.c`` (plain C,
+  binary32 arithmetic as the statement of the problem fixes it: s = amax/448,
+  q = RNE-saturate(x/s) to E4M3). Grouping per 1x128 activation tile and per
+  128x128 weight block: "personal notes concerning the deepseek core
+  readings" (why-be.why-be.co.kr), fine-grained quantization paragraph,
+  Figure 7(a).
+* The GEMM is the plain definition the method approximates: dequantize both
+  operands exactly in float64 (code value times its group's scale) and
+  contract over K, C = A_hat @ W_hat^T. The pages apply the per-group scales
+  along K during dequantization with FP32 accumulation on CUDA cores
+  (Q&A post on xn--9g3bo1gtkw0l8ubf92bgle.kr, paragraph on per-group scaling
+  factors along the inner dimension K; "How Google Is Changing How We Method
+  Deepseek", paragraph on limited accumulation bit width); up to rounding
+  order that is exactly this contraction. The matmul is numpy's float64
+  routine, used as a library primitive.
+* Grouped (MoE) GEMM: the same contraction per expert slice of rows (Q&A
+  post, paragraph on quantizing before the MoE up-projection for FP8 Fprop).
+* Acceptance bound: |C_gpu - C_or| <= 2e-5 * sum_k |A_hat W_hat| + 1e-6, plus
+  2^-8 |C_or| for a bf16 output (statement of the problem).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8bs_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_fp8bs.so")
+
+# Flags that keep every float operation a single IEEE binary32 operation.
+_CFLAGS = ["-std=c11", "-O2", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-fexcess-precision=standard", "-fno-math-errno"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the C half of the oracle with gcc (no CUDA involved)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp"
+        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        i64 = ctypes.c_int64
+        L.fp8o_e4m3_decode.restype = ctypes.c_double
+        L.fp8o_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.fp8o_e4m3_encode.restype = ctypes.c_uint8
+        L.fp8o_e4m3_encode.argtypes = [ctypes.c_float]
+        L.fp8o_group_scale.restype = ctypes.c_float
+        L.fp8o_group_scale.argtypes = [ctypes.c_float]
+        L.fp8o_quantize_value.restype = ctypes.c_uint8
+        L.fp8o_quantize_value.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.fp8o_quantize_act_1x128.restype = None
+        L.fp8o_quantize_act_1x128.argtypes = [u16p, i64, i64, i64, u8p, i64, f32p]
+        L.fp8o_quantize_weight_128x128.restype = None
+        L.fp8o_quantize_weight_128x128.argtypes = [u16p, i64, i64, i64, u8p, i64, f32p]
+        L.fp8o_quantize_pairs.restype = None
+        L.fp8o_quantize_pairs.argtypes = [u16p, u16p, i64, u8p, f32p]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    assert a.flags["C_CONTIGUOUS"] or a.ndim == 0
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# ---------------------------------------------------------------------------
+# E4M3 codec
+# ---------------------------------------------------------------------------
+
+def e4m3_decode(code: int) -> float:
+    return lib().fp8o_e4m3_decode(int(code) & 0xFF)
+
+
+def e4m3_encode(y: float) -> int:
+    return int(lib().fp8o_e4m3_encode(float(np.float32(y))))
+
+
+def e4m3_table() -> np.ndarray:
+    """float64 value of each of the 256 codes (NaN for 0x7F and 0xFF)."""
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def group_scale(amax: float) -> np.float32:
+    return np.float32(lib().fp8o_group_scale(float(np.float32(amax))))
+
+
+def quantize_value(x: float, s: float) -> int:
+    return int(lib().fp8o_quantize_value(float(np.float32(x)), float(np.float32(s))))
+
+
+# ---------------------------------------------------------------------------
+# Quantizers. Inputs are bf16 bit patterns held as uint16 arrays.
+# ---------------------------------------------------------------------------
+
+def quantize_act_1x128(x_bits: np.ndarray):
+    """x_bits: uint16 [M, K] (bf16 patterns) -> (q uint8 [M, K], s float32 [M, K/128])."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), dtype=np.uint8)
+    s = np.empty((M, K // 128), dtype=np.float32)
+    if M and K:
+        lib().fp8o_quantize_act_1x128(_ptr(x_bits, ctypes.c_uint16), M, K, K,
+                                      _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
+    return q, s
+
+
+def quantize_weight_128x128(w_bits: np.ndarray):
+    """w_bits: uint16 [N, K] -> (q uint8 [N, K], s float32 [ceil(N/128), K/128])."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w_bits.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), dtype=np.uint8)
+    s = np.empty(((N + 127) // 128, K // 128), dtype=np.float32)
+    if N and K:
+        lib().fp8o_quantize_weight_128x128(_ptr(w_bits, ctypes.c_uint16), N, K, K,
+                                           _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
+    return q, s
+
+
+def quantize_pairs(amax_bits: np.ndarray, x_bits: np.ndarray):
+    """Codes of x under the scale of amax, element by element."""
+    amax_bits = np.ascontiguousarray(amax_bits, dtype=np.uint16).ravel()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16).ravel()
+    n = x_bits.size
+    q = np.empty(n, dtype=np.uint8)
+    s = np.empty(n, dtype=np.float32)
+    if n:
+        lib().fp8o_quantize_pairs(_ptr(amax_bits, ctypes.c_uint16), _ptr(x_bits, ctypes.c_uint16),
+                                  n, _ptr(q, ctypes.c_uint8), _ptr(s, ctypes.c_float))
+    return q, s
+
+
+# ---------------------------------------------------------------------------
+# Dequantization and the GEMM (float64).
+# ---------------------------------------------------------------------------
+
+_TABLE = None
+
+
+def _table() -> np.ndarray:
+    global _TABLE
+    if _TABLE is None:
+        _TABLE = e4m3_table()
+    return _TABLE
+
+
+def dequant_act(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """A_hat[m, k] = value(q[m, k]) * s[m, k // 128], exact in float64."""
+    M, K = q.shape
+    return _table()[q] * np.repeat(s.astype(np.float64), 128, axis=1)[:, :K]
+
+
+def dequant_weight(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """W_hat[n, k] = value(q[n, k]) * s[n // 128, k // 128], exact in float64."""
+    N, K = q.shape
+    sf = np.repeat(np.repeat(s.astype(np.float64), 128, axis=0), 128, axis=1)[:N, :K]
+    return _table()[q] * sf
+
+
+def gemm(qa, sa, qw, sw):
+    """C_or = A_hat @ W_hat^T and B = |A_hat| @ |W_hat|^T, both float64 [M, N]."""
+    A = dequant_act(qa, sa)
+    W = dequant_weight(qw, sw)
+    return A @ W.T, np.abs(A) @ np.abs(W).T
+
+
+def gemm_entries(qa, sa, qw, sw, rows, cols):
+    """C_or and B at the listed (row, col) pairs only, one dot product each."""
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    A = dequant_act(qa[rows], sa[rows])
+    W = dequant_weight_rows(qw, sw, cols)
+    prod = A * W
+    return prod.sum(axis=1), np.abs(prod).sum(axis=1)
+
+
+def dequant_weight_rows(qw, sw, rows):
+    """W_hat for the listed output channels."""
+    rows = np.asarray(rows)
+    K = qw.shape[1]
+    sf = np.repeat(sw.astype(np.float64)[rows // 128], 128, axis=1)[:, :K]
+    return _table()[qw[rows]] * sf
+
+
+def grouped_gemm(qa, sa, offsets, qw, sw):
+    """Per expert e: rows offsets[e]:offsets[e+1] of A times W_e^T.
+
+    qw: uint8 [E, N, K]; sw: float32 [E, ceil(N/128), K/128]."""
+    E = len(offsets) - 1
+    total = int(offsets[-1])
+    N = qw.shape[1]
+    C = np.zeros((total, N), dtype=np.float64)
+    B = np.zeros((total, N), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            C[lo:hi], B[lo:hi] = gemm(qa[lo:hi], sa[lo:hi], qw[e], sw[e])
+    return C, B
+
+
+def tolerance(C_or: np.ndarray, B: np.ndarray, out_bf16: bool) -> np.ndarray:
+    """Elementwise acceptance bound for a GPU result against C_or."""
+    tol = 2e-5 * B + 1e-6
+    if out_bf16:
+        tol = tol + np.abs(C_or) * 2.0 ** -8
+    return tol
