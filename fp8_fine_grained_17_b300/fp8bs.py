@@ -1,0 +1,184 @@
+"""Python binding of libfp8bs.so (ctypes): argument marshalling only.
+
+Every function named ``fp8bs_*`` here forwards to the C entry point of the
+same name with the tensors' device pointers and sizes; all work runs in the
+library's CUDA kernels. PyTorch supplies device memory and streams only.
+There is no CPU fallback: if the library is missing or a tensor is not on a
+CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8bs.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8bs.h")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OUT_F32, OUT_BF16 = 0, 1
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m fp8_fine_grained_17_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, f32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        st = ctypes.c_int
+        L.fp8bs_quantize_act_1x128.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp]
+        L.fp8bs_quantize_act_1x128.restype = st
+        L.fp8bs_quantize_weight_128x128.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp]
+        L.fp8bs_quantize_weight_128x128.restype = st
+        L.fp8bs_gemm.argtypes = [vp, f32p, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64, vp]
+        L.fp8bs_gemm.restype = st
+        L.fp8bs_grouped_gemm.argtypes = [vp, f32p, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
+                                         i64, i64, i64, vp]
+        L.fp8bs_grouped_gemm.restype = st
+        L.fp8bs_status_string.argtypes = [ctypes.c_int]
+        L.fp8bs_status_string.restype = ctypes.c_char_p
+        L.fp8bs_last_device_error.argtypes = [vp]
+        L.fp8bs_last_device_error.restype = st
+        _lib = L
+    return _lib
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions declared in include/fp8bs.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fp8bs_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().fp8bs_status_string(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("fp8bs works on CUDA tensors only (no CPU path)")
+    return t.data_ptr()
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise Fp8bsError(fn, status)
+
+
+def _row_stride(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def _u8(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+# ---------------------------------------------------------------- C entry points
+
+def fp8bs_quantize_act_1x128(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None):
+    """x bf16 [M, K] -> q e4m3/uint8 [M, K], scale fp32 [M, K/128] (contiguous)."""
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16 and scale.dtype == torch.float32 and scale.is_contiguous()
+    q8 = _u8(q)
+    _check("fp8bs_quantize_act_1x128", lib().fp8bs_quantize_act_1x128(
+        _ptr(x), M, K, _row_stride(x), _ptr(q8), _row_stride(q8), _ptr(scale), _stream(stream)))
+
+
+def fp8bs_quantize_weight_128x128(w: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None):
+    """w bf16 [N, K] -> q [N, K], scale fp32 [ceil(N/128), K/128] (contiguous)."""
+    N, K = w.shape
+    assert w.dtype == torch.bfloat16 and scale.dtype == torch.float32 and scale.is_contiguous()
+    q8 = _u8(q)
+    _check("fp8bs_quantize_weight_128x128", lib().fp8bs_quantize_weight_128x128(
+        _ptr(w), N, K, _row_stride(w), _ptr(q8), _row_stride(q8), _ptr(scale), _stream(stream)))
+
+
+def _out_dtype(c: torch.Tensor) -> int:
+    if c.dtype == torch.float32:
+        return OUT_F32
+    if c.dtype == torch.bfloat16:
+        return OUT_BF16
+    raise ValueError("output must be float32 or bfloat16")
+
+
+def fp8bs_gemm(qa, sa, qw, sw, c, stream=None):
+    """C[M, N] = dequant(qa, sa) @ dequant(qw, sw)^T into c (fp32 or bf16)."""
+    M, K = qa.shape
+    N = qw.shape[0]
+    for t in (qa, sa, qw, sw):
+        assert t.is_contiguous()
+    _check("fp8bs_gemm", lib().fp8bs_gemm(
+        _ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw), _ptr(c), _out_dtype(c),
+        M, N, K, _row_stride(c), _stream(stream)))
+
+
+def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None):
+    """Per expert e: rows offsets[e]:offsets[e+1] of A times W_e^T."""
+    total_M, K = qa.shape
+    E, N, _ = qw.shape
+    assert expert_offsets.dtype == torch.int32 and expert_offsets.numel() == E + 1
+    for t in (qa, sa, qw, sw, expert_offsets):
+        assert t.is_contiguous()
+    _check("fp8bs_grouped_gemm", lib().fp8bs_grouped_gemm(
+        _ptr(_u8(qa)), _ptr(sa), _ptr(expert_offsets), E, total_M, _ptr(_u8(qw)), _ptr(sw),
+        _ptr(c), _out_dtype(c), N, K, _row_stride(c), _stream(stream)))
+
+
+def fp8bs_last_device_error(stream=None) -> int:
+    """Synchronizes the stream; returns (and clears) the device error status."""
+    return lib().fp8bs_last_device_error(_stream(stream))
+
+
+# ------------------------------------------------------ allocating conveniences
+
+def quantize_act(x: torch.Tensor, stream=None):
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
+    fp8bs_quantize_act_1x128(x, q, s, stream)
+    return q, s
+
+
+def quantize_weight(w: torch.Tensor, stream=None):
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8bs_quantize_weight_128x128(w, q, s, stream)
+    return q, s
+
+
+def gemm(qa, sa, qw, sw, out_dtype=torch.bfloat16, stream=None):
+    c = torch.empty((qa.shape[0], qw.shape[0]), dtype=out_dtype, device=qa.device)
+    fp8bs_gemm(qa, sa, qw, sw, c, stream)
+    return c
+
+
+def grouped_gemm(qa, sa, expert_offsets, qw, sw, out_dtype=torch.bfloat16, stream=None):
+    c = torch.zeros((qa.shape[0], qw.shape[1]), dtype=out_dtype, device=qa.device)
+    fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream)
+    return c

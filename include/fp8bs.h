@@ -1,0 +1,157 @@
+/*
+ * fp8bs -- fine-grained block-scaled FP8 GEMM path for B300 (sm_103a).
+ *
+ * C ABI of libfp8bs.so. Plain pointers and sizes only.
+ *
+ * The method (fine-grained FP8 mixed precision):
+ *  - activations are grouped and scaled per 1x128 tile (per token per 128
+ *    channels), weights per 128x128 block (per 128 input channels per 128
+ *    output channels) -- "personal notes concerning the deepseek core
+ *    readings" (why-be.why-be.co.kr), fine-grained quantization paragraph,
+ *    Figure 7(a);
+ *  - each group's maximum magnitude is mapped onto the largest FP8 value and
+ *    the tensor is quantized online with that factor -- Q&A post on
+ *    xn--9g3bo1gtkw0l8ubf92bgle.kr, mixed-precision paragraph;
+ *  - the GEMM multiplies the FP8 operands on tensor cores and applies the
+ *    per-group scales along K on CUDA cores while promoting partial sums to
+ *    FP32 -- same Q&A post, paragraph on per-group scaling factors along K,
+ *    and "How Google Is Changing How We Method Deepseek", paragraph on
+ *    limited accumulation bit width;
+ *  - in MoE, activations are quantized before the up-projection and each
+ *    expert runs an FP8 GEMM (FP8 Fprop) -- Q&A post, paragraph on
+ *    quantizing before the MoE up-projections.
+ *
+ * Numerics fixed by the statement of the problem: FP8 = E4M3 (OCP "FN"
+ * variant, max 448); group scale s = amax / 448 in binary32 (s = 1 when the
+ * group is all zeros); code q = round-to-nearest-even-with-saturation of the
+ * binary32 quotient x / s. The stored scale s is the dequantization
+ * multiplier: value ~= decode(q) * s.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are caller-owned DEVICE memory on the current CUDA
+ *    device. The library allocates and frees nothing and never synchronizes,
+ *    except fp8bs_last_device_error.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.
+ *  - Arguments are validated before anything is launched; a rejected call
+ *    returns FP8BS_ERR_INVALID_ARG or FP8BS_ERR_UNSUPPORTED and touches no
+ *    memory. A launch failure returns FP8BS_ERR_CUDA. Errors detected on the
+ *    device (a bounded wait that expired, bad expert offsets) are reported
+ *    later by fp8bs_last_device_error.
+ *  - M = 0 (or an expert with no rows) is a valid no-op.
+ *  - Inputs must be finite; NaN/Inf inputs are outside the contract.
+ *  - Leading dimensions are in elements; rows must start on 16-byte
+ *    boundaries (pointers 16-byte aligned, ld * element size % 16 == 0).
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *fp8bs_stream_t;
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad stride */
+    FP8BS_ERR_UNSUPPORTED = 2, /* K or N not a multiple of 128, too many experts, wrong GPU */
+    FP8BS_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    FP8BS_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (see last_device_error) */
+} fp8bs_status;
+
+typedef enum { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 } fp8bs_out_dtype;
+
+/*
+ * Activation quantization, 1x128 tiles (per token per 128 channels).
+ *
+ *   x      bf16  [M, K], row stride ldx (elements)            (input)
+ *   q      e4m3  [M, K], row stride ldq (bytes)               (output codes)
+ *   scale  fp32  [M, K/128] row-major, contiguous             (output)
+ *
+ * For every row m and group g: amax = max_k |x[m, 128g+k]|,
+ * s = scale[m, g] = amax/448 (1 if amax == 0), q[m, 128g+k] = E4M3(x/s).
+ * K % 128 == 0 (else FP8BS_ERR_UNSUPPORTED). Codes and scales are
+ * bit-identical to the definition above.
+ */
+fp8bs_status fp8bs_quantize_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                      uint8_t *q, int64_t ldq, float *scale,
+                                      fp8bs_stream_t stream);
+
+/*
+ * Weight quantization, 128x128 blocks (per 128 input x 128 output channels).
+ *
+ *   w      bf16  [N, K] (output channel x input channel), row stride ldw
+ *   q      e4m3  [N, K], row stride ldq
+ *   scale  fp32  [ceil(N/128), K/128] row-major, contiguous
+ *
+ * Block (nb, kb) covers rows 128nb..128nb+127 (only those < N) and columns
+ * 128kb..128kb+127; its amax, scale and codes follow the same rule as the
+ * activation tiles. K % 128 == 0 (else FP8BS_ERR_UNSUPPORTED). Stacked
+ * expert weights [E, N, K] with N % 128 == 0 quantize as one [E*N, K] call.
+ */
+fp8bs_status fp8bs_quantize_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                           uint8_t *q, int64_t ldq, float *scale,
+                                           fp8bs_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM: C[M, N] = A_hat * W_hat^T, where
+ * A_hat[m, k] = decode(qa[m, k]) * sa[m, k/128] and
+ * W_hat[n, k] = decode(qw[n, k]) * sw[n/128, k/128].
+ *
+ *   qa  e4m3 [M, K] contiguous          sa  fp32 [M, K/128] contiguous
+ *   qw  e4m3 [N, K] contiguous          sw  fp32 [N/128, K/128] contiguous
+ *   c   [M, N] with row stride ldc, fp32 or bf16 (RNE) per out_dtype
+ *
+ * Each 128-wide K chunk is multiplied on the tensor cores into an FP32
+ * partial and then promoted: acc += sa[m, kb] * sw[n/128, kb] * partial.
+ * Requires K % 128 == 0 and N % 128 == 0 (else FP8BS_ERR_UNSUPPORTED); any
+ * M >= 0. K == 0 writes zeros. Accuracy: |C - C_exact| <=
+ * 2e-5 * sum_k |A_hat W_hat| + 1e-6 (+ 2^-8 |C| for bf16 output).
+ */
+fp8bs_status fp8bs_gemm(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
+                        void *c, fp8bs_out_dtype out_dtype, int64_t M, int64_t N, int64_t K,
+                        int64_t ldc, fp8bs_stream_t stream);
+
+/*
+ * Grouped (MoE) GEMM: for each expert e, rows r in
+ * [expert_offsets[e], expert_offsets[e+1]) of A are multiplied by W_e:
+ * C[r, :] = A_hat[r, :] * W_hat_e^T.
+ *
+ *   qa, sa           as in fp8bs_gemm, with total_M rows
+ *   expert_offsets   int32 [E+1], DEVICE memory: offsets[0] = 0,
+ *                    nondecreasing, offsets[E] <= total_M. Read on the
+ *                    device (no host synchronization); invalid offsets make
+ *                    the kernel write nothing and are reported by
+ *                    fp8bs_last_device_error as FP8BS_ERR_INVALID_ARG.
+ *   qw               e4m3 [E, N, K] contiguous
+ *   sw               fp32 [E, N/128, K/128] contiguous
+ *   c                [total_M, N], row stride ldc; rows not covered by any
+ *                    expert are left untouched
+ *
+ * 1 <= E <= 1024; K % 128 == 0, N % 128 == 0. Same accuracy as fp8bs_gemm.
+ */
+fp8bs_status fp8bs_grouped_gemm(const uint8_t *qa, const float *sa, const int32_t *expert_offsets,
+                                int32_t E, int64_t total_M, const uint8_t *qw, const float *sw,
+                                void *c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
+                                int64_t ldc, fp8bs_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *fp8bs_status_string(fp8bs_status status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error
+ * word: FP8BS_ERR_TIMEOUT if a bounded device wait expired since the last
+ * call, FP8BS_ERR_INVALID_ARG if a grouped GEMM saw invalid offsets,
+ * FP8BS_ERR_CUDA if the synchronization itself failed, else FP8BS_OK.
+ */
+fp8bs_status fp8bs_last_device_error(fp8bs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,102 @@
+"""GPU parity of the block-scaled FP8 GEMM against the float64 oracle.
+
+Bound (fixed by the statement of the problem), element by element:
+|C_gpu - C_or| <= 2e-5 * sum_k |A_hat W_hat| + 1e-6, plus 2^-8 |C_or| for bf16."""
+import numpy as np
+import pytest
+import torch
+
+from fp8_fine_grained_17_b300 import fp8bs
+from fp8_fine_grained_17_b300 import workloads as wl
+from helpers import check_codes, check_gemm, gpu_quant_act, gpu_quant_weight
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(orc, a_bits, w_bits, out_dtype, check_quant=True):
+    qa, sa = gpu_quant_act(a_bits)
+    qw, sw = gpu_quant_weight(w_bits)
+    qa_o, sa_o = orc.quantize_act_1x128(a_bits)
+    qw_o, sw_o = orc.quantize_weight_128x128(w_bits)
+    if check_quant:
+        check_codes(qa, sa, qa_o, sa_o)
+        check_codes(qw, sw, qw_o, sw_o)
+    c = fp8bs.gemm(qa, sa, qw, sw, out_dtype)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(qa_o, sa_o, qw_o, sw_o)
+    return check_gemm(c, C_or, B, out_dtype == torch.bfloat16)
+
+
+def test_reference_case_f32(orc):
+    """Quantize + GEMM, M=128, N=256, K=512, fp32 output, seed 0."""
+    d = wl.cfg0(0)
+    _run(orc, d.a_bits, d.w_bits, torch.float32)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 128, 128), (5, 256, 128), (127, 128, 256), (129, 384, 512),
+    (300, 640, 1024), (257, 1152, 384), (128, 256, 4096),
+])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_shapes(orc, M, N, K, out):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    _run(orc, a, w, out)
+
+
+def test_per_chunk_scales_honoured(orc):
+    """Chunk kb of A is scaled by 4^kb and W's blocks by distinct factors."""
+    rng = np.random.default_rng(3)
+    M, N, K = 256, 512, 1024
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    a *= np.repeat(4.0 ** np.arange(K // 128), 128)[None, :].astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w *= np.repeat(np.repeat(2.0 ** rng.integers(-8, 8, (N // 128, K // 128)), 128, 0), 128, 1).astype(np.float32)
+    _run(orc, wl.bf16_bits(a), wl.bf16_bits(w), torch.float32)
+
+
+def test_zero_and_identity(orc):
+    M, K = 200, 512
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    a[:, 256:384] = 0.0
+    w = np.eye(K, dtype=np.float32)
+    _run(orc, wl.bf16_bits(a), wl.bf16_bits(w), torch.float32)
+
+
+def test_k_zero_writes_zeros():
+    qa = torch.empty((5, 0), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((5, 0), dtype=torch.float32, device="cuda")
+    qw = torch.empty((256, 0), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((2, 0), dtype=torch.float32, device="cuda")
+    c = torch.full((5, 256), 7.0, dtype=torch.float32, device="cuda")
+    fp8bs.fp8bs_gemm(qa, sa, qw, sw, c)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)
+
+
+def test_strided_output_untouched_margin(orc):
+    rng = np.random.default_rng(5)
+    M, N, K, ldc = 130, 256, 256, 320
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = gpu_quant_act(a)
+    qw, sw = gpu_quant_weight(w)
+    cbuf = torch.full((M + 1, ldc), -3.0, dtype=torch.float32, device="cuda")
+    fp8bs.fp8bs_gemm(qa, sa, qw, sw, cbuf[:M, :N])
+    torch.cuda.synchronize()
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
+    check_gemm(cbuf[:M, :N], C_or, B, False)
+    assert torch.all(cbuf[:M, N:] == -3.0) and torch.all(cbuf[M] == -3.0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", ["cfg2", "cfg3"])
+def test_full_workloads(orc, cfg):
+    """M=4096,N=7168,K=2048 (outliers x50) and M=4096,N=4096,K=7168, bf16
+    output: every output element against the float64 oracle."""
+    d = getattr(wl, cfg)(0)
+    worst = _run(orc, d.a_bits, d.w_bits, torch.bfloat16)
+    print(f"{cfg}: worst err/tol = {worst:.3g}")

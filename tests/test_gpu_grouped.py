@@ -1,0 +1,111 @@
+"""GPU parity of the grouped (MoE up-projection) GEMM against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from fp8_fine_grained_17_b300 import fp8bs
+from fp8_fine_grained_17_b300 import workloads as wl
+from helpers import check_codes, check_gemm, gpu_quant_act, gpu_quant_weight
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant_experts(orc, w_bits, check=True):
+    """Per-expert weight quantization on the GPU as one [E*N, K] call."""
+    E, N, K = w_bits.shape
+    qw, sw = gpu_quant_weight(w_bits.reshape(E * N, K))
+    if check:
+        q_o, s_o = orc.quantize_weight_128x128(w_bits.reshape(E * N, K))
+        check_codes(qw, sw, q_o, s_o)
+    return qw.view(E, N, K), sw.view(E, N // 128, K // 128)
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([3, 0, 5, 1], 128, 256),
+    ([0, 0, 0, 200], 256, 384),
+    ([130, 1, 0, 257, 64], 384, 512),
+    ([1], 128, 128),
+    ([0, 128, 0], 640, 256),
+])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_grouped_small(orc, counts, N, K, out):
+    d = wl.moe(seed=sum(counts) + N, N=N, K=K, counts=counts)
+    qa, sa = gpu_quant_act(d.a_bits)
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    check_codes(qa, sa, qa_o, sa_o)
+    qw, sw = _quant_experts(orc, d.w_bits)
+    off = torch.from_numpy(d.offsets).cuda()
+    c = fp8bs.grouped_gemm(qa, sa, off, qw, sw, out)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    E, N, K = d.w_bits.shape
+    q_o, s_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K),
+                               s_o.reshape(E, N // 128, K // 128))
+    check_gemm(c, C_or, B, out == torch.bfloat16)
+
+
+def test_rows_outside_experts_untouched(orc):
+    """offsets[E] < total_M: trailing rows are not written."""
+    d = wl.moe(seed=9, N=256, K=256, counts=[70, 40])
+    extra = 30
+    a_bits = np.concatenate([d.a_bits, d.a_bits[:extra]])
+    qa, sa = gpu_quant_act(a_bits)
+    qw, sw = _quant_experts(orc, d.w_bits, check=False)
+    c = torch.full((a_bits.shape[0], 256), 5.0, dtype=torch.float32, device="cuda")
+    fp8bs.fp8bs_grouped_gemm(qa, sa, torch.from_numpy(d.offsets).cuda(), qw, sw, c)
+    torch.cuda.synchronize()
+    assert torch.all(c[110:] == 5.0)
+    q_o, s_o = orc.quantize_act_1x128(a_bits[:110])
+    wq, ws = orc.quantize_weight_128x128(d.w_bits.reshape(-1, 256))
+    C_or, B = orc.grouped_gemm(q_o, s_o, d.offsets, wq.reshape(2, 256, 256), ws.reshape(2, 2, 2))
+    check_gemm(c[:110], C_or, B, False)
+
+
+def test_bad_offsets_reported(orc):
+    """Decreasing offsets: nothing is written and the device error says so."""
+    d = wl.moe(seed=10, N=128, K=128, counts=[10, 10])
+    qa, sa = gpu_quant_act(d.a_bits)
+    qw, sw = _quant_experts(orc, d.w_bits, check=False)
+    c = torch.full((20, 128), 2.0, dtype=torch.float32, device="cuda")
+    bad = torch.tensor([0, 15, 12], dtype=torch.int32, device="cuda")
+    fp8bs.fp8bs_grouped_gemm(qa, sa, bad, qw, sw, c)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.ERR_INVALID_ARG
+    assert torch.all(c == 2.0)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK      # cleared by the read
+
+
+@pytest.mark.slow
+def test_moe_full_workload_sampled(orc):
+    """32 experts, N=4096, K=7168, rows from the seeded top-8 router; the full
+    launch, checked on sampled outputs (rows of every expert x two 128-column
+    blocks per expert) against per-entry float64 dot products."""
+    d = wl.moe(seed=0)
+    E, N, K = d.w_bits.shape
+    qa, sa = gpu_quant_act(d.a_bits)
+    qw, sw = gpu_quant_weight(d.w_bits.reshape(E * N, K))
+    off = torch.from_numpy(d.offsets).cuda()
+    c = fp8bs.grouped_gemm(qa, sa, off, qw.view(E, N, K), sw.view(E, N // 128, K // 128))
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    c = c.float().cpu().numpy()
+    qa_h, sa_h = qa.cpu().numpy(), sa.cpu().numpy()
+    rng = np.random.default_rng(1)
+    worst = 0.0
+    for e in range(E):
+        lo, hi = int(d.offsets[e]), int(d.offsets[e + 1])
+        if hi == lo:
+            continue
+        rows = np.unique(rng.integers(lo, hi, min(16, hi - lo)))
+        q_rows, s_rows = orc.quantize_act_1x128(d.a_bits[rows])
+        check_codes(qa[rows], sa[rows], q_rows, s_rows)
+        for nb in rng.choice(N // 128, 2, replace=False):
+            blk = d.w_bits[e, nb * 128:(nb + 1) * 128]
+            q_b, s_b = orc.quantize_weight_128x128(blk)
+            check_codes(qw[e * N + nb * 128: e * N + (nb + 1) * 128], sw[e * (N // 128) + nb:e * (N // 128) + nb + 1], q_b, s_b)
+            rr, cc = np.meshgrid(np.arange(len(rows)), np.arange(128), indexing="ij")
+            C_or, B = orc.gemm_entries(q_rows, s_rows, q_b, s_b, rr.ravel(), cc.ravel())
+            got = c[rows[rr.ravel()], nb * 128 + cc.ravel()]
+            tol = 2e-5 * B + 1e-6 + np.abs(C_or) * 2.0 ** -8
+            err = np.abs(got - C_or)
+            assert np.all(err <= tol), (e, nb, np.max(err / tol))
+            worst = max(worst, float(np.max(err / tol)))
+    print(f"moe sampled worst err/tol {worst:.3g}")
