@@ -2,26 +2,35 @@
 """Benchmark of the fine-grained FP8 GEMM path on B300.
 
 One step = one FP8 forward of a linear layer at M=4096, N=4096, K=7168 from
-bf16 inputs: activation quantization (1x128 tiles), weight quantization
-(128x128 blocks), and the block-scaled GEMM with bf16 output. The headline
-value is GEMM TFLOP/s over the whole step. The same run also measures the
-activation quantizer alone on [16384, 7168] (GB/s) and the MoE grouped GEMM
-(32 experts, N=4096, K=7168, seeded top-8 routing) as extra keys.
+bf16 inputs already resident in HBM: activation quantization (1x128 tiles),
+weight quantization (128x128 blocks) and the block-scaled GEMM with bf16
+output. The headline value is GEMM FLOPs over the whole step's time
+(TFLOP/s). The same run also measures, as extra keys:
+
+* the activation quantizer alone on [16384, 7168] with 0.5% outlier channels
+  (GB/s against the HBM roofline),
+* the GEMM M=4096, N=7168, K=2048 with 0.5% outlier channels x50,
+* the MoE grouped GEMM (32 experts, N=4096, K=7168, seeded top-8 routing),
+* the end-to-end step from pinned host buffers (`e2e`),
+* the CPU oracle on a bounded sample (`cpu_baseline`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--part all|step|act_quant|gemm2|moe] [--skip-cpu]
 
 With --gpus N > 1 (launched by torchrun) every rank runs the same step on its
 own GPU with no collective on the data path (independent replicas, weak
 scaling); the value is the sum of all ranks' work over the slowest rank's time.
+`--impl reference` times the CPU oracle on the host cores instead.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
+import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -35,8 +44,29 @@ from fp8_fine_grained_17_b300 import workloads as wl  # noqa: E402
 L2_BYTES = 126 * 2 ** 20
 METRIC = "FP8 block-scaled GEMM TFLOP/s (% of dense FP8 peak); act-quant HBM GB/s"
 UNIT = "TFLOP/s"
-WORKLOAD = "GEMM M=4096,N=4096,K=7168: A bf16 ~N(0,1), W bf16 ~N(0,0.02), block-quantized to E4M3, bf16 out"
+WORKLOAD = ("GEMM M=4096,N=4096,K=7168: A bf16 ~N(0,1), W bf16 ~N(0,0.02), "
+            "block-quantized to E4M3, bf16 out")
 M3, N3, K3 = 4096, 4096, 7168
+CSRC = os.path.join(ROOT, "fp8_fine_grained_17_b300", "csrc")
+
+# DRAM bytes (read + write) per launch from one ncu capture of each kernel,
+# keyed by the SHA-256 prefix of the kernel's source file at capture time. A
+# kernel whose source has changed since reports traffic = null.
+NCU_TRAFFIC = {
+    # kernel: (source file, sha256 prefix, workload, bytes per launch, capture)
+}
+
+
+def _src_hash(fname: str) -> str:
+    with open(os.path.join(CSRC, fname), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel: str, workload: str):
+    ent = NCU_TRAFFIC.get(kernel)
+    if ent is None or ent[2] != workload or _src_hash(ent[0]) != ent[1]:
+        return None
+    return ent[3]
 
 
 def _peaks():
@@ -50,80 +80,98 @@ def _peaks():
             "source": "fallback"}
 
 
+def _fp8_peak(peaks):
+    """Dense FP8 peak: measured bf16 cuBLAS burst x the nominal FP8/BF16 ratio
+    (4.5 / 2.25 PFLOP/s)."""
+    return peaks["bf16_tflops"] * 2.0
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples SM clock, power and throttle reasons with nvidia-smi while it
+    is open (one line every 50 ms)."""
 
-    REASONS = {
-        "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
-    }
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NAMED = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, device_index: int, period_s: float = 0.002):
-        self.samples = []
-        self.reasons = set()
-        self.max_mhz = None
-        self._stop = threading.Event()
-        self._period = period_s
+    def __init__(self, device: torch.device, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", f"-lms={period_ms}"]
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.cmd.append("--id=" + (uuid if uuid.startswith("GPU-") else "GPU-" + uuid))
         except Exception:
-            self._nvml = None
-        self._t = threading.Thread(target=self._run, daemon=True)
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self._nvml.nvmlDeviceGetClockInfo(self._h, self._nvml.NVML_CLOCK_SM))
-                r = self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for name, bit in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(name)
-            except Exception:
-                pass
-            time.sleep(self._period)
+            pass
+        self.proc = None
+        self.lines = []
 
     def __enter__(self):
-        if self._nvml is not None:
-            self._t.start()
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self._stop.set()
-        if self._nvml is not None:
-            self._t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples), "source": "nvml"}
+        mhz, max_mhz, watts, reasons = [], None, [], set()
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                cur, mx, w = float(f[0]), float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            mhz.append(cur)
+            max_mhz = mx
+            watts.append(w)
+            for name, val in zip(self.NAMED, f[4:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max_mhz,
+                "sm_mhz_min": min(mhz) if mhz else None,
+                "power_w_max": max(watts) if watts else None,
+                "reasons": sorted(reasons), "samples": len(mhz),
+                "source": "nvidia-smi -lms 50 over warm-up + timed region"}
+
+
+def _events(n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
+
+
+def _median_ms(evs):
+    return float(np.median([a.elapsed_time(b) for a, b in evs]))
 
 
 # --------------------------------------------------------------------- our arm
 
-def _dense_inputs(n_sets: int, dev):
+def _dense_inputs(n_sets: int, dev, cfg):
     """n_sets independent seeded (A, W) bf16 pairs on the device."""
     sets = []
     for i in range(n_sets):
-        d = wl.cfg3(seed=i)
+        d = cfg(seed=i)
         sets.append((wl.bits_to_torch(d.a_bits).to(dev), wl.bits_to_torch(d.w_bits).to(dev)))
     return sets
 
 
-def run_ours(args, rank, world):
-    from fp8_fine_grained_17_b300 import fp8bs
-
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(dev)
-    peaks = _peaks()
-
+def bench_step(fp8bs, dev, stream, peaks, args, world):
+    """The headline: quantize A + quantize W + GEMM at 4096 x 4096 x 7168."""
     step_in_bytes = 2 * (M3 * K3 + N3 * K3)
     n_sets = max(2, -(-3 * L2_BYTES // step_in_bytes))
-    sets = _dense_inputs(n_sets, dev)
+    sets = _dense_inputs(n_sets, dev, wl.cfg3)
     qa = torch.empty((M3, K3), dtype=torch.uint8, device=dev)
     sa = torch.empty((M3, K3 // 128), dtype=torch.float32, device=dev)
     qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
@@ -144,25 +192,25 @@ def run_ours(args, rank, world):
         if ev is not None:
             ev[3].record(stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i)
-    stream.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                step(i)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             t0.record(stream)
             for i in range(args.steps):
                 step(i, evs[i])
             t1.record(stream)
         stream.synchronize()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     elapsed_ms = t0.elapsed_time(t1)
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -175,74 +223,107 @@ def run_ours(args, rank, world):
                     for e in evs])
     t_qa, t_qw, t_gemm = per.mean(axis=0)
     flops = 2.0 * M3 * N3 * K3
-    ms_per_step = elapsed_ms / args.steps
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
-    fp8_peak = peaks["bf16_tflops"] * 2.0      # measured bf16 burst x nominal fp8/bf16 ratio (4.5/2.25)
+    fp8_peak = _fp8_peak(peaks)
     gemm_tflops = flops / (t_gemm * 1e-3) / 1e12
     qa_bytes = M3 * K3 * 2 + M3 * K3 + M3 * (K3 // 128) * 4
     qw_bytes = N3 * K3 * 2 + N3 * K3 + (N3 // 128) * (K3 // 128) * 4
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded numpy N(0,1) activations, N(0,0.02) weights, bf16)",
-        "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "out": "bf16",
-                   "step": "quantize A 1x128 + quantize W 128x128 + block-scaled GEMM",
-                   "l2": f"inputs rotated over {n_sets} seeded sets "
-                         f"({n_sets * step_in_bytes / 1e6:.0f} MB > 126 MB L2), no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel",
+    del sets
+    return {
+        "elapsed_ms": elapsed_ms,
+        "value": world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12,
+        "n_sets": n_sets, "set_bytes": n_sets * step_in_bytes,
+        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel<dense>",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                     "traffic": None,
-                     "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x 2 (nominal fp8/bf16)",
+                     "traffic": _traffic("fp8_gemm_kernel", "gemm 4096x4096x7168"),
+                     "algorithmic": f"2*M*N*K = {flops:.4g} flop per launch / mean launch time "
+                                    f"{t_gemm * 1e3:.2f} us (CUDA events, {args.steps} launches)",
+                     "peak_note": f"of {peaks['source']}: bf16 cuBLAS burst "
+                                  f"{peaks['bf16_tflops']} x 2 (nominal fp8/bf16)",
                      "frac_of_nominal_4500": round(gemm_tflops / 4500.0, 4)},
         "kernels": {
-            "quantize_act_1x128": {"ms": round(t_qa, 4), "GB/s": round(qa_bytes / (t_qa * 1e-3) / 1e9, 1),
-                                   "frac_hbm": round(qa_bytes / (t_qa * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
-            "quantize_weight_128x128": {"ms": round(t_qw, 4), "GB/s": round(qw_bytes / (t_qw * 1e-3) / 1e9, 1),
-                                        "frac_hbm": round(qw_bytes / (t_qw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
-            "gemm": {"ms": round(t_gemm, 4), "TFLOP/s": round(gemm_tflops, 1)},
+            "quantize_act_1x128": {
+                "us": round(t_qa * 1e3, 2), "GB/s": round(qa_bytes / (t_qa * 1e-3) / 1e9, 1),
+                "frac_hbm": round(qa_bytes / (t_qa * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+            "quantize_weight_128x128": {
+                "us": round(t_qw * 1e3, 2), "GB/s": round(qw_bytes / (t_qw * 1e-3) / 1e9, 1),
+                "frac_hbm": round(qw_bytes / (t_qw * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+            "gemm": {"us": round(t_gemm * 1e3, 2), "TFLOP/s": round(gemm_tflops, 1)},
         },
-        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
-    del sets
-    torch.cuda.empty_cache()
-    if not args.skip_extras:
-        result["act_quant"] = bench_act_quant(fp8bs, dev, stream, peaks, args)
-        result["moe_grouped"] = bench_moe(fp8bs, dev, stream, peaks, args)
-        result["e2e"] = bench_e2e(fp8bs, dev, stream, args)
-    return result
 
 
 def bench_act_quant(fp8bs, dev, stream, peaks, args):
-    """Activation quantizer alone on [16384, 7168] with 0.5% outlier channels x100."""
-    d = wl.cfg1(0)
-    x = wl.bits_to_torch(d.a_bits).to(dev)
-    M, K = x.shape
+    """Activation quantizer alone on [16384, 7168] with 0.5% outlier channels
+    x100, alternating between two seeded inputs (470 MB > L2)."""
+    xs = [wl.bits_to_torch(wl.cfg1(s).a_bits).to(dev) for s in (0, 1)]
+    M, K = xs[0].shape
     q = torch.empty((M, K), dtype=torch.uint8, device=dev)
     s = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            fp8bs.fp8bs_quantize_act_1x128(x, q, s, stream)
-    n = max(20, args.steps)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(max(3, args.warmup)):
+            fp8bs.fp8bs_quantize_act_1x128(xs[i % 2], q, s, stream)
+    n = max(20, min(args.steps, 200))
+    evs = _events(n)
     with torch.cuda.stream(stream):
-        for e0, e1 in evs:
+        for i, (e0, e1) in enumerate(evs):
             e0.record(stream)
-            fp8bs.fp8bs_quantize_act_1x128(x, q, s, stream)
+            fp8bs.fp8bs_quantize_act_1x128(xs[i % 2], q, s, stream)
             e1.record(stream)
     stream.synchronize()
-    ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
-    nbytes = M * K * 2 + M * K + M * (K // 128) * 4
+    ms = _median_ms(evs)
+    groups = M * (K // 128)
+    nbytes = groups * (256 + 128 + 4)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": "act-quant [16384,7168] bf16, 36 outlier channels x100", "ms": round(ms, 4),
-            "GB/s": round(gbs, 1), "bytes": nbytes,
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8000": round(gbs / 8000.0, 4)},
-            "l2": "input 235 MB > 126 MB L2", "timing": f"median of {n} launches"}
+    return {"workload": "act-quant [16384,7168] bf16, 36 outlier channels x100",
+            "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "bytes": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "quantize_act_kernel",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": _traffic("quantize_act_kernel", "act-quant 16384x7168"),
+                         "algorithmic": f"{groups} groups x 388 B (256 B read, 128 B codes, "
+                                        f"4 B scale)",
+                         "peak_note": f"of {peaks['source']} copy bandwidth",
+                         "frac_of_8000": round(gbs / 8000.0, 4)},
+            "l2": "two 235 MB inputs alternated (> 126 MB L2)",
+            "timing": f"median of {n} launches"}
+
+
+def bench_gemm2(fp8bs, dev, stream, peaks, args):
+    """GEMM M=4096, N=7168, K=2048 (0.5% outlier channels x50), pre-quantized
+    operands, bf16 out; operands of 3 seeded sets rotated."""
+    qs = []
+    for seed in range(3):
+        d = wl.cfg2(seed)
+        qa, sa = fp8bs.quantize_act(wl.bits_to_torch(d.a_bits).to(dev), stream)
+        qw, sw = fp8bs.quantize_weight(wl.bits_to_torch(d.w_bits).to(dev), stream)
+        qs.append((qa, sa, qw, sw))
+    M, K = qs[0][0].shape
+    N = qs[0][2].shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
+    n = max(20, min(args.steps, 200))
+    evs = _events(n)
+    with torch.cuda.stream(stream):
+        for i, (e0, e1) in enumerate(evs):
+            e0.record(stream)
+            fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
+            e1.record(stream)
+    stream.synchronize()
+    assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
+    ms = _median_ms(evs)
+    flops = 2.0 * M * N * K
+    tf = flops / (ms * 1e-3) / 1e12
+    fp8_peak = _fp8_peak(peaks)
+    return {"workload": "GEMM M=4096,N=7168,K=2048, 0.5% outlier channels x50, bf16 out",
+            "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
+                         "frac_of_nominal_4500": round(tf / 4500.0, 4)},
+            "timing": f"median of {n} launches, 3 operand sets rotated"}
 
 
 def bench_moe(fp8bs, dev, stream, peaks, args):
@@ -251,8 +332,8 @@ def bench_moe(fp8bs, dev, stream, peaks, args):
     E, N, K = len(d.counts), d.N, d.K
     rng_w = torch.Generator(device=dev)
     rng_w.manual_seed(0)
-    # Expert weights: codes and scales drawn on the device from a seeded
-    # generator (the kernel's time does not depend on the values).
+    # Expert weights: finite E4M3 codes and positive scales drawn on the device
+    # from a seeded generator (the kernel's time does not depend on the values).
     qw = torch.randint(0, 0x7F, (E, N, K), dtype=torch.uint8, device=dev, generator=rng_w)
     sw = torch.rand((E, N // 128, K // 128), device=dev, generator=rng_w) * 1e-4
     x = wl.bits_to_torch(d.a_bits).to(dev)
@@ -263,8 +344,8 @@ def bench_moe(fp8bs, dev, stream, peaks, args):
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             fp8bs.fp8bs_grouped_gemm(qa, sa, off, qw, sw, c, stream)
-    n = max(10, args.steps // 2)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    n = max(10, min(args.steps, 100))
+    evs = _events(n)
     with torch.cuda.stream(stream):
         for e0, e1 in evs:
             e0.record(stream)
@@ -272,17 +353,17 @@ def bench_moe(fp8bs, dev, stream, peaks, args):
             e1.record(stream)
     stream.synchronize()
     assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
-    ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+    ms = _median_ms(evs)
     flops = 2.0 * total * N * K
     tflops = flops / (ms * 1e-3) / 1e12
     wbytes = E * N * K
-    fp8_peak = peaks["bf16_tflops"] * 2.0
+    fp8_peak = _fp8_peak(peaks)
     t_bound = max(flops / (fp8_peak * 1e12), wbytes / (peaks["hbm_gbs"] * 1e9))
     return {"workload": f"MoE grouped GEMM 32 experts N=4096 K=7168, rows {total} "
                         f"(max {int(d.counts.max())}, min {int(d.counts.min())})",
-            "ms": round(ms, 4), "TFLOP/s": round(tflops, 1), "weight_bytes": wbytes,
-            "roofline": {"bound": "tensor+weight stream", "achieved_ms": round(ms, 4),
-                         "bound_ms": round(t_bound * 1e3, 4), "frac": round(t_bound * 1e3 / ms, 4),
+            "us": round(ms * 1e3, 2), "TFLOP/s": round(tflops, 1), "weight_bytes": wbytes,
+            "roofline": {"bound": "max(tensor, weight stream)", "achieved_us": round(ms * 1e3, 2),
+                         "bound_us": round(t_bound * 1e6, 2), "frac": round(t_bound * 1e3 / ms, 4),
                          "tensor_frac": round(tflops / fp8_peak, 4)},
             "timing": f"median of {n} launches; weights 940 MB > L2"}
 
@@ -314,7 +395,7 @@ def bench_e2e(fp8bs, dev, stream, args):
         for _ in range(max(3, args.warmup)):
             step()
         stream.synchronize()
-        n = max(10, args.steps // 2)
+        n = max(10, min(args.steps, 50))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n):
@@ -325,10 +406,65 @@ def bench_e2e(fp8bs, dev, stream, args):
     flops = 2.0 * M3 * N3 * K3
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": 2 * (M3 * K3 + N3 * K3), "d2h_bytes_per_step": 2 * M3 * N3,
-            "ms_per_step": round(ms, 4), "steps": n}
+            "ms_per_step": round(ms, 4), "steps": n,
+            "path": "pinned host A, W -> H2D -> quantize A, quantize W, GEMM -> D2H C"}
+
+
+def run_ours(args, world):
+    from fp8_fine_grained_17_b300 import fp8bs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    parts = {"all": ("step", "act_quant", "gemm2", "moe", "e2e")}.get(args.part, (args.part,))
+
+    result = {}
+    if "step" in parts:
+        s = bench_step(fp8bs, dev, stream, peaks, args, world)
+        result = {
+            "metric": METRIC, "value": round(s["value"], 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(s["elapsed_ms"] / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded numpy N(0,1) activations, N(0,0.02) weights, bf16)",
+            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "out": "bf16",
+                       "step": "quantize A 1x128 + quantize W 128x128 + block-scaled GEMM",
+                       "l2": f"inputs rotated over {s['n_sets']} seeded sets "
+                             f"({s['set_bytes'] / 1e6:.0f} MB > 126 MB L2), no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": s["roofline"],
+            "kernels": s["kernels"],
+            "gpu_launches": 3 * args.steps,
+            "clocks": s["clocks"],
+        }
+        torch.cuda.empty_cache()
+    if "act_quant" in parts:
+        result["act_quant"] = bench_act_quant(fp8bs, dev, stream, peaks, args)
+        torch.cuda.empty_cache()
+    if "gemm2" in parts:
+        result["gemm_4096x7168x2048"] = bench_gemm2(fp8bs, dev, stream, peaks, args)
+        torch.cuda.empty_cache()
+    if "moe" in parts:
+        result["moe_grouped"] = bench_moe(fp8bs, dev, stream, peaks, args)
+        torch.cuda.empty_cache()
+    if "e2e" in parts:
+        result["e2e"] = bench_e2e(fp8bs, dev, stream, args)
+    return result
 
 
 # --------------------------------------------------------------- oracle (CPU)
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d["num_threads"] for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
 
 def _oracle_step(orc, a_bits, w_bits):
     qa, sa = orc.quantize_act_1x128(a_bits)
@@ -336,69 +472,75 @@ def _oracle_step(orc, a_bits, w_bits):
     orc.gemm(qa, sa, qw, sw)
 
 
-def cpu_baseline(budget_s: float = 15.0, rows: int | None = None):
+def _oracle_sample(orc, budget_s: float):
+    """Rows of A for one oracle step of about budget_s seconds: the step is
+    quantize A[rows, 7168] + quantize W[4096, 7168] + float64 GEMM
+    rows x 4096 x 7168, so its time is affine in rows; fit it from two runs."""
+    d = wl.cfg3(seed=0)
+    ts = []
+    for r in (8, 32):
+        t = time.perf_counter()
+        _oracle_step(orc, d.a_bits[:r], d.w_bits)
+        ts.append(time.perf_counter() - t)
+    per_row = max((ts[1] - ts[0]) / 24, 1e-6)
+    fixed = max(ts[0] - 8 * per_row, 0.0)
+    rows = int(np.clip((budget_s - fixed) / per_row, 8, M3))
+    return d, rows
+
+
+def cpu_baseline(budget_s: float = 15.0):
     """The oracle (C quantizers + float64 numpy GEMM) on a bounded sample of
-    the step: the first `rows` rows of A and the first rows of W, so the
-    sample is (rows x 4096-column-slice) of the same GEMM; TFLOP/s scaled by
-    the sample's own FLOPs."""
+    the step: the first `rows` rows of A with all of W, i.e. a rows x 4096 x
+    7168 slice of the same GEMM; TFLOP/s counts the sample's own FLOPs."""
     from oracle import oracle as orc
-    d = wl.dense("sample", 256, N3, K3, seed=0)
-    a_bits, w_bits = d.a_bits, d.w_bits
-    # calibrate on a small slice
+    d, rows = _oracle_sample(orc, budget_s)
     t = time.perf_counter()
-    _oracle_step(orc, a_bits[:16], w_bits[:256])
-    t_small = time.perf_counter() - t
-    if rows is None:
-        rows = int(np.clip(16 * budget_s / max(t_small, 1e-3) / 16, 16, 256))
-    n_cols = 256 * max(1, min(N3 // 256, int(budget_s / max(t_small, 1e-3))))
-    t = time.perf_counter()
-    _oracle_step(orc, a_bits[:rows], w_bits[:n_cols])
+    _oracle_step(orc, d.a_bits[:rows], d.w_bits)
     dt = time.perf_counter() - t
-    flops = 2.0 * rows * n_cols * K3
-    threads = int(os.environ.get("OMP_NUM_THREADS", 0)) or os.cpu_count()
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"quantize A[{rows},{K3}] + W[{n_cols},{K3}] (C, 1 thread) and float64 GEMM "
-                      f"{rows}x{n_cols}x{K3} (numpy BLAS) in {dt:.2f} s",
+    flops = 2.0 * rows * N3 * K3
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"quantize A[{rows},{K3}] + W[{N3},{K3}] (plain C, 1 thread) and float64 "
+                      f"GEMM {rows}x{N3}x{K3} (numpy BLAS, {_blas_threads()} threads) in {dt:.2f} s",
             "seconds": round(dt, 2)}
 
 
-def run_reference(args, rank):
-    """The oracle timed on the host cores, K timed steps of a bounded sample."""
+def run_reference(args):
+    """The oracle timed on the host cores: W + K steps, each a bounded sample
+    (rows x 4096 x 7168 slice) of the headline step."""
     from oracle import oracle as orc
-    d = wl.dense("sample", 64, N3, K3, seed=0)
-    budget_per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))
-    t = time.perf_counter()
-    _oracle_step(orc, d.a_bits[:8], d.w_bits[:256])
-    t_small = time.perf_counter() - t
-    scale = max(1.0, budget_per_step / max(t_small, 1e-3))
-    rows = int(min(64, 8 * scale ** 0.5))
-    n_cols = int(min(N3, 256 * max(1, int(scale ** 0.5))) // 256 * 256)
+    per_step = float(np.clip(150.0 / max(1, args.steps + args.warmup), 0.5, 15.0))
+    d, rows = _oracle_sample(orc, per_step)
     for _ in range(args.warmup):
-        _oracle_step(orc, d.a_bits[:rows], d.w_bits[:n_cols])
+        _oracle_step(orc, d.a_bits[:rows], d.w_bits)
     t = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(orc, d.a_bits[:rows], d.w_bits[:n_cols])
+        _oracle_step(orc, d.a_bits[:rows], d.w_bits)
     dt = time.perf_counter() - t
-    flops = 2.0 * rows * n_cols * K3
+    flops = 2.0 * rows * N3 * K3
     value = flops * args.steps / dt / 1e12
-    cores = int(os.environ.get("OMP_NUM_THREADS", 0)) or os.cpu_count()
-    sample = f"quantize A[{rows},{K3}] + W[{n_cols},{K3}] + float64 GEMM {rows}x{n_cols}x{K3} per step"
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3},
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    cores = _blas_threads()
+    sample = (f"per step: quantize A[{rows},{K3}] + W[{N3},{K3}] (plain C, 1 thread) + float64 "
+              f"GEMM {rows}x{N3}x{K3} (numpy BLAS, {cores} threads)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-extras", action="store_true", help="headline step only")
+    ap.add_argument("--part", choices=["all", "step", "act_quant", "gemm2", "moe", "e2e"],
+                    default="all", help="which measurements to run (profiling uses one)")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle CPU baseline")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -408,15 +550,17 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, rank)), flush=True)
+            print(json.dumps(run_reference(args)), flush=True)
         return
 
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    res = run_ours(args, rank, world)
+        if args.part != "step":
+            args.part = "step"       # extras are single-GPU measurements
+    res = run_ours(args, world)
     if rank == 0:
-        if world == 1 and not args.skip_cpu:
+        if world == 1 and not args.skip_cpu and args.part == "all":
             res["cpu_baseline"] = cpu_baseline()
         print(json.dumps(res), flush=True)
     if world > 1:
