@@ -112,6 +112,26 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// ------------------------------------------------------------------ cp.async
+
+// 4-byte asynchronous global -> shared copy (L1-allocating).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive once on `bar` when all earlier cp.async of this thread have landed;
+// the arrival is one of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
@@ -248,6 +268,74 @@ template <int N>
 __device__ __forceinline__ void regs_inc()
 {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------- packed FP32 math
+//
+// sm_100+ executes some binary32 operations on register pairs: each half is
+// one IEEE operation rounded to nearest even, subnormals kept (no .ftz).
+
+// Two binary32 values in one 64-bit register pair (lo in the low half).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t pack_b32x2(uint32_t lo, uint32_t hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// a * b per half.
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// a * b + c per half, fused (one rounding).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// (a0, a1) = fma((p0, p1), s2, (a0, a1)) with the accumulators held as two
+// scalars and the partial sums as raw binary32 bits.
+__device__ __forceinline__ void ffma2f(float& a0, float& a1, uint32_t p0, uint32_t p1, uint64_t s2)
+{
+    asm("{\n\t.reg .b64 t, a;\n\t"
+        "mov.b64 t, {%2, %3};\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "fma.rn.f32x2 a, t, %4, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(p0), "r"(p1), "l"(s2));
+}
+
+// ------------------------------------------------------------- packed bf16
+
+// Per 16-bit half: max(|a|, |b|) in the low 15 bits (the sign bit of each
+// half is the XOR of the operands' signs and must be masked off by the
+// caller). Subnormal bf16 values are kept.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // --------------------------------------------------------------- conversions

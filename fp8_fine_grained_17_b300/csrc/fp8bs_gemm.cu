@@ -21,11 +21,16 @@
 //               (K = 32 each) per chunk into one of two 256-column FP32 TMEM
 //               buffers, overwriting it (the chunk's partial P_kb).
 //   warp 2      TMEM allocator (512 columns).
-//   warp 3      grouped GEMM: builds the expert tile table.
+//   warp 3      scale loader: copies each chunk's 128 activation scales and
+//               two weight-block scales into an 8-slot shared-memory ring
+//               with cp.async (grouped GEMM: first builds the expert tile
+//               table), running up to 8 chunks ahead of the promotion warps.
 //   warps 4-11  promotion: each thread owns one row and 128 columns; per
-//               chunk it reads P_kb from TMEM (tcgen05.ld), frees the buffer,
-//               and accumulates acc += (sa * sw) * P_kb in FP32 registers.
-//               After the last chunk it converts and stores its row segment.
+//               chunk it reads P_kb from TMEM (tcgen05.ld, the next 32
+//               columns in flight while the current ones are accumulated),
+//               frees the buffer, and accumulates acc += (sa * sw) * P_kb in
+//               FP32 registers. After the last chunk it converts and stores
+//               its row segment.
 // The two TMEM buffers let the tensor cores compute chunk kb+1 while the
 // promotion warps drain chunk kb.
 #include <cstdint>
@@ -44,6 +49,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int kStages = 4;
+constexpr int kScaleStages = 8;
 constexpr int kABytes = BM * BK;
 constexpr int kBBytes = BN * BK;
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -62,6 +68,10 @@ struct __align__(1024) Smem {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
+    uint64_t scale_full[kScaleStages];    // 32 cp.async arrivals (one per loader lane)
+    uint64_t scale_empty[kScaleStages];   // 8 arrivals (one per promotion warp)
+    float scale_a[kScaleStages][BM];      // sa[m0 + r, kb]
+    float scale_w[kScaleStages][4];       // sw[e, n0/128 + h, kb], h = 0, 1
     uint32_t tmem_base;
     int abort;
     int num_tiles;
@@ -83,7 +93,6 @@ struct Params {
     int out_bf16;
     const int32_t* offsets;   // grouped only
     int E;
-    int dense_tiles;
     unsigned int* err;
 };
 
@@ -95,53 +104,44 @@ struct Tile {
     int b_row0;        // first row of the W tile in the [E*N, K] weight matrix
 };
 
-template <bool kGrouped>
+// Tile t of the launch: the expert e with tile_start[e] <= t < tile_start[e+1]
+// (binary search; a dense launch is one expert covering all rows), then the
+// m-tile and n-tile within that expert, m-tiles fastest.
 __device__ __forceinline__ Tile decode_tile(const Smem& sm, const Params& p, int t)
 {
-    Tile tile;
-    if (!kGrouped) {
-        const int m_tiles = static_cast<int>((p.rows + BM - 1) / BM);
-        const int mt = t % m_tiles;
-        const int nt = t / m_tiles;
-        tile.m0 = static_cast<int64_t>(mt) * BM;
-        tile.row_end = p.rows;
-        tile.n0 = nt * BN;
-        tile.expert = 0;
-        tile.b_row0 = tile.n0;
-    } else {
-        // expert e with tile_start[e] <= t < tile_start[e+1]
-        int lo = 0, hi = p.E;   // invariant: tile_start[lo] <= t < tile_start[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (sm.tile_start[mid] <= t)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        const int e = lo;
-        const int local = t - sm.tile_start[e];
-        const int rows_e = sm.row_start[e + 1] - sm.row_start[e];
-        const int mt_e = (rows_e + BM - 1) / BM;
-        const int mt = local % mt_e;
-        const int nt = local / mt_e;
-        tile.m0 = sm.row_start[e] + static_cast<int64_t>(mt) * BM;
-        tile.row_end = sm.row_start[e + 1];
-        tile.n0 = nt * BN;
-        tile.expert = e;
-        tile.b_row0 = e * p.N + tile.n0;
+    int lo = 0, hi = p.E;   // invariant: tile_start[lo] <= t < tile_start[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.tile_start[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
     }
+    const int e = lo;
+    const int local = t - sm.tile_start[e];
+    const int rows_e = sm.row_start[e + 1] - sm.row_start[e];
+    const int mt_e = (rows_e + BM - 1) / BM;
+    const int mt = local % mt_e;
+    const int nt = local / mt_e;
+    Tile tile;
+    tile.m0 = sm.row_start[e] + static_cast<int64_t>(mt) * BM;
+    tile.row_end = sm.row_start[e + 1];
+    tile.n0 = nt * BN;
+    tile.expert = e;
+    tile.b_row0 = e * p.N + tile.n0;
     return tile;
 }
 
-// Warp 3 of a grouped launch: copy and validate expert_offsets, then build
-// tile_start[] (exclusive prefix sum of m-tiles x n-tiles per expert).
+// Warp 3: copy and validate expert_offsets (a dense launch uses {0, M}),
+// then build tile_start[] (exclusive prefix sum of m-tiles x n-tiles per
+// expert).
 __device__ void build_expert_table(Smem& sm, const Params& p, int lane)
 {
     bool ok = true;
     for (int base = 0; base <= p.E; base += 32) {
         const int i = base + lane;
         if (i <= p.E)
-            sm.row_start[i] = p.offsets[i];
+            sm.row_start[i] = p.offsets != nullptr ? p.offsets[i] : (i == 0 ? 0 : static_cast<int>(p.rows));
     }
     __syncwarp();
     int carry = 0;
@@ -181,7 +181,6 @@ __device__ void build_expert_table(Smem& sm, const Params& p, int lane)
     }
 }
 
-template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p)
@@ -203,9 +202,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             mbar_init(smem_addr(&sm.tmem_empty[b]), 8);   // one arrive per promotion warp
         }
         mbar_init(smem_addr(&sm.drain), 1);
+        for (int s = 0; s < kScaleStages; ++s) {
+            mbar_init(smem_addr(&sm.scale_full[s]), 32);
+            mbar_init(smem_addr(&sm.scale_empty[s]), 8);
+        }
         sm.abort = 0;
-        if (!kGrouped)
-            sm.num_tiles = p.dense_tiles;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0 && p.KB > 0) {
@@ -216,7 +217,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (kGrouped && warp == 3)
+    if (warp == 3)
         build_expert_table(sm, p, lane);
     tc_fence_before();
     __syncthreads();
@@ -233,7 +234,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             uint32_t chunk = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile tile = decode_tile<kGrouped>(sm, p, t);
+                const Tile tile = decode_tile(sm, p, t);
                 for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
                     const uint32_t s = chunk % kStages;
                     const uint32_t ph = (chunk / kStages) & 1u;
@@ -284,6 +285,40 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // All MMAs issued by this thread complete before TMEM is released.
             mma_commit(smem_addr(&sm.drain));
             mbar_wait_drain(smem_addr(&sm.drain), 0, kWaitLimitNs, p.err);
+        } else if (warp == 3) {
+            // ---------------------------------------------------- scale loader
+            uint32_t chunk = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const Tile tile = decode_tile(sm, p, t);
+                // Rows past the tile's end read a valid row; their products
+                // are never stored.
+                const float* src_a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t row = tile.m0 + lane + 32 * i;
+                    src_a[i] = p.sa + (row < p.rows ? row : p.rows - 1) * p.KB;
+                }
+                const int nbh = min(tile.n0 / 128 + (lane & 1), p.NB - 1);
+                const float* src_w = p.sw + (static_cast<int64_t>(tile.expert) * p.NB + nbh) * p.KB;
+                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
+                    const uint32_t s = chunk % kScaleStages;
+                    const uint32_t ph = (chunk / kScaleStages) & 1u;
+                    const bool ready =
+                        mbar_wait(smem_addr(&sm.scale_empty[s]), ph ^ 1u, abort_flag, p.err);
+                    if (!__all_sync(0xFFFFFFFFu, ready)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        cp_async_4(smem_addr(&sm.scale_a[s][lane + 32 * i]), src_a[i] + kb);
+                    if (lane < 2)
+                        cp_async_4(smem_addr(&sm.scale_w[s][lane]), src_w + kb);
+                    cp_async_arrive_noinc(smem_addr(&sm.scale_full[s]));
+                }
+            }
+            cp_async_wait_all();
         }
     } else {
         regs_inc<kEpilogueRegs>();
@@ -294,29 +329,32 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         uint32_t chunk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile tile = decode_tile<kGrouped>(sm, p, t);
+            const Tile tile = decode_tile(sm, p, t);
             const int64_t row = tile.m0 + r;
             const int n_col = tile.n0 + half * 128;
             const bool live = row < tile.row_end && n_col < p.N;
-            const float* sa_row = p.sa + (live ? row : 0) * p.KB;
-            const float* sw_row =
-                p.sw + (static_cast<int64_t>(tile.expert) * p.NB + (live ? n_col / 128 : 0)) * p.KB;
 
-            float acc[128];
+            // 128 FP32 accumulators as 64 pairs for the packed FMA pipe.
+            float2 acc[64];
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-                acc[i] = 0.0f;
-            float next_scale = (live && p.KB > 0) ? __ldg(sa_row) * __ldg(sw_row) : 0.0f;
-
+            for (int i = 0; i < 64; ++i)
+                acc[i] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
             for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                const float scale = next_scale;
-                if (live && kb + 1 < p.KB)
-                    next_scale = __ldg(sa_row + kb + 1) * __ldg(sw_row + kb + 1);
+                const uint32_t ss = chunk % kScaleStages;
+                const uint32_t sph = (chunk / kScaleStages) & 1u;
                 const uint32_t b = chunk & 1u;
                 const uint32_t tph = (chunk >> 1) & 1u;
-                // The warp continues only if every lane saw the phase complete:
-                // the TMEM loads below are warp-collective.
-                const bool ready = mbar_wait(smem_addr(&sm.tmem_full[b]), tph, abort_flag, p.err);
+                // The warp continues only if every lane saw the phases
+                // complete: the TMEM loads below are warp-collective.
+                bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), sph, abort_flag, p.err);
+                float scale = 0.0f;
+                if (ready)
+                    scale = sm.scale_a[ss][r] * sm.scale_w[ss][half];
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&sm.scale_empty[ss]));
+                ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), tph, abort_flag, p.err);
                 if (!__all_sync(0xFFFFFFFFu, ready)) {
                     ok = false;
                     break;
@@ -324,19 +362,43 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + half * 128;
+                const float2 scale2 = make_float2(scale, scale);
+                // Column blocks 0..3 of 32: the load of block j+1 is in flight
+                // while block j is accumulated.
+                uint32_t va[32], vb[32];
+                tmem_ld_32x32b_x32(taddr, va);
+                tmem_ld_wait(va);
+                tmem_ld_32x32b_x32(taddr + 32, vb);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + 32 * j, v);
-                    tmem_ld_wait(v);
+                for (int i = 0; i < 16; ++i)
+                    acc[0 + i] = __ffma2_rn(
+                        make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])),
+                        scale2, acc[0 + i]);
+                tmem_ld_wait(vb);
+                tmem_ld_32x32b_x32(taddr + 64, va);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[32 * j + i] = fmaf(__uint_as_float(v[i]), scale, acc[32 * j + i]);
-                }
+                for (int i = 0; i < 16; ++i)
+                    acc[16 + i] = __ffma2_rn(
+                        make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])),
+                        scale2, acc[16 + i]);
+                tmem_ld_wait(va);
+                tmem_ld_32x32b_x32(taddr + 96, vb);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    acc[32 + i] = __ffma2_rn(
+                        make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])),
+                        scale2, acc[32 + i]);
+                tmem_ld_wait(vb);
+                // Every TMEM read of this buffer is complete: hand it back.
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&sm.tmem_empty[b]));
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    acc[48 + i] = __ffma2_rn(
+                        make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])),
+                        scale2, acc[48 + i]);
             }
             if (ok && live) {
                 if (p.out_bf16) {
@@ -344,10 +406,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         uint4 pk;
-                        __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[8 * i + 0], acc[8 * i + 1]);
-                        __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[8 * i + 2], acc[8 * i + 3]);
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[8 * i + 4], acc[8 * i + 5]);
-                        __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[8 * i + 6], acc[8 * i + 7]);
+                        __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
+                        __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
+                        __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
+                        __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
                         memcpy(&pk.x, &h0, 4);
                         memcpy(&pk.y, &h1, 4);
                         memcpy(&pk.z, &h2, 4);
@@ -358,8 +420,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        reinterpret_cast<float4*>(dst)[i] =
-                            make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                        reinterpret_cast<float4*>(dst)[i] = make_float4(
+                            acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
                 }
             }
         }
@@ -409,7 +471,6 @@ bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
     return r == CUDA_SUCCESS;
 }
 
-template <bool kGrouped>
 fp8bs_status configure_once(int device)
 {
     static std::mutex mu;
@@ -418,7 +479,7 @@ fp8bs_status configure_once(int device)
     if (device < 0 || device >= 64)
         return FP8BS_ERR_CUDA;
     if (!done[device]) {
-        if (cudaFuncSetAttribute(fp8_gemm_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes)) != cudaSuccess) {
             cudaGetLastError();
             return FP8BS_ERR_CUDA;
@@ -428,7 +489,6 @@ fp8bs_status configure_once(int device)
     return FP8BS_OK;
 }
 
-template <bool kGrouped>
 fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
                     int64_t K, int64_t tile_bound, cudaStream_t stream)
 {
@@ -446,13 +506,13 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
         if (!encode_operand(&map_a, qa, rows, K, BM) || !encode_operand(&map_b, qw, w_rows, K, BN))
             return FP8BS_ERR_CUDA;
     }
-    st = configure_once<kGrouped>(info.device);
+    st = configure_once(info.device);
     if (st != FP8BS_OK)
         return st;
     const int grid = static_cast<int>(tile_bound < info.sm_count ? tile_bound : info.sm_count);
     if (grid <= 0)
         return FP8BS_OK;
-    fp8_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
+    fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
     return launch_status();
 }
 
@@ -496,7 +556,7 @@ extern "C" fp8bs_status fp8bs_gemm(const uint8_t* qa, const float* sa, const uin
         return st;
     const int64_t m_tiles = (M + BM - 1) / BM;
     const int64_t n_tiles = (N + BN - 1) / BN;
-    if (m_tiles * n_tiles > 0x7FFFFFFF)
+    if (M > 0x7FFFFFFF || m_tiles * n_tiles > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
 
     Params p{};
@@ -512,8 +572,7 @@ extern "C" fp8bs_status fp8bs_gemm(const uint8_t* qa, const float* sa, const uin
     p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
     p.offsets = nullptr;
     p.E = 1;
-    p.dense_tiles = static_cast<int>(m_tiles * n_tiles);
-    return launch<false>(qa, M, qw, N, p, K, m_tiles * n_tiles,
+    return launch(qa, M, qw, N, p, K, m_tiles * n_tiles,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -554,7 +613,6 @@ extern "C" fp8bs_status fp8bs_grouped_gemm(const uint8_t* qa, const float* sa,
     p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
     p.offsets = expert_offsets;
     p.E = E;
-    p.dense_tiles = 0;
-    return launch<true>(qa, total_M, qw, static_cast<int64_t>(E) * N, p, K, tile_bound,
+    return launch(qa, total_M, qw, static_cast<int64_t>(E) * N, p, K, tile_bound,
                         reinterpret_cast<cudaStream_t>(stream));
 }

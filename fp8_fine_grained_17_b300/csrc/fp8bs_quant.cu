@@ -10,13 +10,18 @@
 // is E4M3(round_f32(x / s)). A full-precision division per element would cost
 // more than the memory traffic, so the quotient is formed from the correctly
 // rounded reciprocal r = 1/s and one residual correction (Markstein's method:
-// y0 = x*r, e = fma(-y0, s, x), y = fma(e, r, y0)), which yields the
+// y0 = x*r, e = x - y0*s (fused), y = e*r + y0 (fused)), which yields the
 // correctly rounded quotient whenever no intermediate underflows. Where the
-// quotient is tiny enough for the residual to underflow the E4M3 code is 0
-// either way, except for the sign of zero, which is restored from x. Groups
-// with amax below 2^-100 (s near the binary32 subnormal range) take a true
-// IEEE division per element instead. This is checked against the
-// definition over every (bf16 amax, bf16 x) pair by the tests.
+// quotient is tiny enough for the residual to underflow, its E4M3 code is 0
+// either way; only the sign of zero can come out wrong (x = -0 gives +0), so
+// every code's sign bit is OR-ed with the sign bit of x, which is the sign
+// the exact quotient has. Groups with 0 < amax < 2^-100 (s near the binary32
+// subnormal range) take a true IEEE division per element instead. The tests
+// check this against the definition over every (bf16 amax, bf16 x) pair.
+//
+// The per-element arithmetic runs on packed pairs (sm_100+ binary32x2 mul /
+// fma, bf16x2 magnitude max), and the per-group scalar work (amax/448 and its
+// reciprocal) is done once per group, spread over the lanes that share it.
 #include <cstdint>
 
 #include "fp8bs_device.cuh"
@@ -28,113 +33,160 @@ namespace {
 constexpr float kE4M3Max = 448.0f;
 constexpr float kFastDivMinAmax = 0x1p-100f;
 
-struct GroupDivider {
+// Scale of a group and the reciprocal used by the fast quotient; r == 0
+// selects the exact-division path.
+struct Divider {
     float s;
     float r;
-    bool fast;
 };
 
-__device__ __forceinline__ GroupDivider make_divider(float amax)
+__device__ __forceinline__ Divider make_divider(float amax)
 {
-    GroupDivider d;
+    Divider d;
     d.s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
-    d.r = __frcp_rn(d.s);
-    d.fast = amax >= kFastDivMinAmax;
+    d.r = (amax == 0.0f || amax >= kFastDivMinAmax) ? __frcp_rn(d.s) : 0.0f;
     return d;
 }
 
-// round_f32(x / s), see the file comment.
-__device__ __forceinline__ float divide(float x, const GroupDivider& d)
+// Largest |x| of a bf16 group fragment held as packed words, as the 16-bit
+// pattern of a non-negative bf16 (integer order = numeric order).
+__device__ __forceinline__ uint32_t absmax_words(const uint4* v, int n)
 {
-    if (d.fast) {
-        const float y0 = __fmul_rn(x, d.r);
-        const float e = __fmaf_rn(-y0, d.s, x);
-        return copysignf(__fmaf_rn(e, d.r, y0), x);
-    }
-    return __fdiv_rn(x, d.s);
+    uint32_t m = 0;
+    for (int j = 0; j < n; ++j)
+        m = absmax_bf16x2(m, absmax_bf16x2(absmax_bf16x2(v[j].x, v[j].y),
+                                           absmax_bf16x2(v[j].z, v[j].w)));
+    m &= 0x7FFF7FFFu;
+    return max(m & 0xFFFFu, m >> 16);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
-__device__ __forceinline__ float absmax_pair(float m, uint32_t w)
+// Sign bits of the 4 bf16 values in (w0, w1), placed on the sign bits of 4
+// E4M3 bytes.
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t w0, uint32_t w1)
 {
-    return fmaxf(m, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
+// 2 bf16 (one word) -> 2 E4M3 codes in the low 16 bits, fast quotient.
+__device__ __forceinline__ uint32_t quantize2_fast(uint32_t w, uint64_t ns2, uint64_t r2)
+{
+    const uint64_t x = pack_b32x2(w << 16, w & 0xFFFF0000u);
+    const uint64_t y0 = mul_f32x2(x, r2);
+    const uint64_t e = fma_f32x2(y0, ns2, x);     // x - y0 * s
+    const float2 y = unpack_f32x2(fma_f32x2(e, r2, y0));
+    return cvt_e4m3x2(y.x, y.y);
+}
+
+// Same with a true IEEE division per element.
+__device__ __forceinline__ uint32_t quantize2_exact(uint32_t w, float s)
+{
+    return cvt_e4m3x2(__fdiv_rn(__uint_as_float(w << 16), s),
+                      __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
 }
 
 // 8 bf16 (one uint4) -> 8 E4M3 codes (one uint2).
-__device__ __forceinline__ uint2 quantize8(const uint4& v, const GroupDivider& d)
+__device__ __forceinline__ uint2 quantize8(const uint4& v, const Divider& d)
 {
-    const uint32_t c0 = cvt_e4m3x2(divide(bf16_lo(v.x), d), divide(bf16_hi(v.x), d));
-    const uint32_t c1 = cvt_e4m3x2(divide(bf16_lo(v.y), d), divide(bf16_hi(v.y), d));
-    const uint32_t c2 = cvt_e4m3x2(divide(bf16_lo(v.z), d), divide(bf16_hi(v.z), d));
-    const uint32_t c3 = cvt_e4m3x2(divide(bf16_lo(v.w), d), divide(bf16_hi(v.w), d));
-    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
-}
-
-__device__ __forceinline__ float absmax8(float m, const uint4& v)
-{
-    m = absmax_pair(m, v.x);
-    m = absmax_pair(m, v.y);
-    m = absmax_pair(m, v.z);
-    return absmax_pair(m, v.w);
+    uint32_t c0, c1, c2, c3;
+    if (d.r != 0.0f) {
+        const uint64_t ns2 = pack_f32x2(-d.s, -d.s);
+        const uint64_t r2 = pack_f32x2(d.r, d.r);
+        c0 = quantize2_fast(v.x, ns2, r2);
+        c1 = quantize2_fast(v.y, ns2, r2);
+        c2 = quantize2_fast(v.z, ns2, r2);
+        c3 = quantize2_fast(v.w, ns2, r2);
+    } else {
+        c0 = quantize2_exact(v.x, d.s);
+        c1 = quantize2_exact(v.y, d.s);
+        c2 = quantize2_exact(v.z, d.s);
+        c3 = quantize2_exact(v.w, d.s);
+    }
+    return make_uint2(__byte_perm(c0, c1, 0x5410) | sign_bytes(v.x, v.y),
+                      __byte_perm(c2, c3, 0x5410) | sign_bytes(v.z, v.w));
 }
 
 // ---------------------------------------------------------------------------
 // Activation quantizer.
 //
-// Four consecutive lanes own one 1x128 group (256 bytes of bf16): lane
-// quarter t loads the 16-byte chunks t, t+4, t+8, t+12 of the group, so one
-// warp-wide load instruction touches 8 groups x 64 contiguous bytes, i.e.
-// whole 32-byte sectors. The group amax is combined with two xor-shuffles.
-// A warp handles kUnroll x 8 groups per iteration of a grid-stride loop;
-// all loads of an iteration are issued before any arithmetic.
+// Four consecutive lanes (a quad) own four consecutive 1x128 groups per
+// iteration; lane t of the quad loads the 16-byte chunks t, t+4, t+8, t+12 of
+// each group, so one warp-wide load instruction touches 8 groups x 64
+// contiguous bytes. The quad's four partial maxima are reduced with a
+// transposing exchange (3 shuffles) that leaves group t's amax in lane t;
+// lane t computes that group's scale and reciprocal and writes the scale
+// (the warp writes 32 consecutive scales), and the quad broadcasts them. All
+// loads of an iteration (256 B per lane) are issued before any arithmetic.
+// kContiguous: rows are back to back (ld == K), so group g starts at element
+// 128 g and no row/column split is needed.
 // ---------------------------------------------------------------------------
 constexpr int kActThreads = 256;
-constexpr int kActUnroll = 2;
 
+template <bool kContiguous>
 __global__ void __launch_bounds__(kActThreads)
 quantize_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
                     int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
                     int64_t total_groups)
 {
     const int lane = threadIdx.x & 31;
-    const int quarter = lane & 3;
+    const int t = lane & 3;
+    const int quad_base = lane & ~3;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kActThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kActThreads) >> 5;
-    const int64_t per_iter = 8 * kActUnroll;
 
-    for (int64_t base = warp * per_iter; base < total_groups; base += n_warps * per_iter) {
-        uint4 v[kActUnroll][4];
-        int64_t row[kActUnroll], col[kActUnroll];
-        bool valid[kActUnroll];
+    for (int64_t base = warp * 32; base < total_groups; base += n_warps * 32) {
+        uint4 v[4][4];
+        int64_t xoff[4], qoff[4];
+        bool valid[4];
 #pragma unroll
-        for (int u = 0; u < kActUnroll; ++u) {
-            const int64_t grp = base + u * 8 + (lane >> 2);
-            valid[u] = grp < total_groups;
-            row[u] = valid[u] ? grp / groups_per_row : 0;
-            col[u] = valid[u] ? (grp - row[u] * groups_per_row) * 128 : 0;
-            const uint4* src = reinterpret_cast<const uint4*>(x + row[u] * ldx + col[u]) + quarter;
+        for (int u = 0; u < 4; ++u) {
+            const int64_t g = base + quad_base + u;
+            valid[u] = g < total_groups;
+            if (kContiguous) {
+                xoff[u] = g * 128;
+                qoff[u] = g * 128;
+            } else {
+                const int64_t row = valid[u] ? g / groups_per_row : 0;
+                const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
+                xoff[u] = row * ldx + col;
+                qoff[u] = row * ldq + col;
+            }
+            const uint4* src = reinterpret_cast<const uint4*>(x + (valid[u] ? xoff[u] : 0)) + t;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
         }
+
+        uint32_t m[4];
 #pragma unroll
-        for (int u = 0; u < kActUnroll; ++u) {
-            float amax = 0.0f;
+        for (int u = 0; u < 4; ++u)
+            m[u] = absmax_words(v[u], 4);
+        // Transposing max-exchange: after it lane t holds group t's amax.
+        const bool b1 = (t & 2) != 0, b0 = (t & 1) != 0;
+        uint32_t k[2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                amax = absmax8(amax, v[u][j]);
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            const GroupDivider d = make_divider(amax);
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b1 ? m[i] : m[2 + i], 2);
+            k[i] = max(b1 ? m[2 + i] : m[i], recv);
+        }
+        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b0 ? k[0] : k[1], 1);
+        const uint32_t mine = max(b0 ? k[1] : k[0], recv);
+
+        const Divider own = make_divider(bf16_bits_to_f32(mine));
+        if (base + lane < total_groups)
+            scale[base + lane] = own.s;   // scale is [M, K/128] row-major: index = g
+
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            Divider d;
+            d.s = __shfl_sync(0xFFFFFFFFu, own.s, quad_base + u);
+            d.r = __shfl_sync(0xFFFFFFFFu, own.r, quad_base + u);
             if (valid[u]) {
-                uint8_t* dst = q + row[u] * ldq + col[u] + quarter * 8;
+                uint8_t* dst = q + qoff[u] + t * 8;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint2*>(dst + 32 * j) = quantize8(v[u][j], d);
-                if (quarter == 0)
-                    scale[row[u] * groups_per_row + col[u] / 128] = d.s;
+                    __stcs(reinterpret_cast<uint2*>(dst + 32 * j), quantize8(v[u][j], d));
             }
         }
     }
@@ -144,8 +196,9 @@ quantize_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __rest
 // Weight quantizer: one 256-thread CTA per 128x128 block. Thread t holds the
 // 16-byte chunk (t & 15) of rows 16i + t/16, i = 0..7, so each warp load
 // instruction covers two whole 256-byte block rows. The block amax is reduced
-// with shuffles and through shared memory; the codes are written from the
-// registers that still hold the inputs.
+// with a warp max-reduction and shared memory; one thread computes the
+// scale and reciprocal, and the codes are written from the registers that
+// still hold the inputs.
 // ---------------------------------------------------------------------------
 constexpr int kWThreads = 256;
 
@@ -154,7 +207,8 @@ quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
                        uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
                        int64_t groups_per_row)
 {
-    __shared__ float warp_max[kWThreads / 32];
+    __shared__ uint32_t warp_max[kWThreads / 32];
+    __shared__ Divider block_div;
     const int t = threadIdx.x;
     const int64_t kb = blockIdx.x;
     const int64_t nb = blockIdx.y;
@@ -162,50 +216,50 @@ quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
     const int64_t col = kb * 128 + chunk * 8;
 
     uint4 v[8];
-    float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t n = nb * 128 + i * 16 + (t >> 4);
         v[i] = n < N ? __ldcs(reinterpret_cast<const uint4*>(w + n * ldw + col))
                      : make_uint4(0, 0, 0, 0);
-        amax = absmax8(amax, v[i]);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, absmax_words(v, 8));
     if ((t & 31) == 0)
-        warp_max[t >> 5] = amax;
+        warp_max[t >> 5] = m;
     __syncthreads();
-    amax = warp_max[0];
+    if (t == 0) {
+        uint32_t a = warp_max[0];
 #pragma unroll
-    for (int i = 1; i < kWThreads / 32; ++i)
-        amax = fmaxf(amax, warp_max[i]);
-
-    const GroupDivider d = make_divider(amax);
+        for (int i = 1; i < kWThreads / 32; ++i)
+            a = max(a, warp_max[i]);
+        const Divider d = make_divider(bf16_bits_to_f32(a));
+        block_div = d;
+        scale[nb * groups_per_row + kb] = d.s;
+    }
+    __syncthreads();
+    const Divider d = block_div;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t n = nb * 128 + i * 16 + (t >> 4);
         if (n < N)
-            *reinterpret_cast<uint2*>(q + n * ldq + col) = quantize8(v[i], d);
+            __stcs(reinterpret_cast<uint2*>(q + n * ldq + col), quantize8(v[i], d));
     }
-    if (t == 0)
-        scale[nb * groups_per_row + kb] = d.s;
 }
 
+template <bool kContiguous>
 int act_grid(const DeviceInfo& info, int64_t total_groups)
 {
     static int blocks_per_sm = 0;
     if (blocks_per_sm == 0) {
         int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_act_kernel, kActThreads, 0) !=
-                cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_act_kernel<kContiguous>,
+                                                          kActThreads, 0) != cudaSuccess ||
             b <= 0) {
             cudaGetLastError();
-            b = 4;
+            b = 2;
         }
         blocks_per_sm = b;
     }
-    const int64_t groups_per_block = (kActThreads / 32) * 8 * kActUnroll;
+    const int64_t groups_per_block = (kActThreads / 32) * 32;
     const int64_t needed = (total_groups + groups_per_block - 1) / groups_per_block;
     const int64_t full = static_cast<int64_t>(info.sm_count) * blocks_per_sm;
     return static_cast<int>(needed < full ? needed : full);
@@ -239,9 +293,15 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
 
     const int64_t G = K / 128;
     const int64_t total = M * G;
-    const int grid = act_grid(info, total);
-    quantize_act_kernel<<<grid, kActThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), ldx, q, ldq, scale, G, total);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (ldx == K && ldq == K) {
+        quantize_act_kernel<true><<<act_grid<true>(info, total), kActThreads, 0, s>>>(
+            xb, ldx, q, ldq, scale, G, total);
+    } else {
+        quantize_act_kernel<false><<<act_grid<false>(info, total), kActThreads, 0, s>>>(
+            xb, ldx, q, ldq, scale, G, total);
+    }
     return launch_status();
 }
 
