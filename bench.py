@@ -53,7 +53,11 @@ CSRC = os.path.join(ROOT, "fp8_fine_grained_17_b300", "csrc")
 # keyed by the SHA-256 prefix of the kernel's source file at capture time. A
 # kernel whose source has changed since reports traffic = null.
 NCU_TRAFFIC = {
-    # kernel: (source file, sha256 prefix, workload, bytes per launch, capture)
+    # kernel: (source file, sha256 prefix, workload, bytes per launch)
+    "fp8_gemm_kernel": ("fp8bs_gemm.cu", "d57f4ede952e8051", "gemm 4096x4096x7168",
+                        59.844864e6 + 9.684480e6),
+    "quantize_act_kernel": ("fp8bs_quant.cu", "aad4b3d82d693e71", "act-quant 16384x7168",
+                            234.938368e6 + 77.691392e6),
 }
 
 
@@ -491,9 +495,11 @@ def _oracle_sample(orc, budget_s: float):
 def cpu_baseline(budget_s: float = 15.0):
     """The oracle (C quantizers + float64 numpy GEMM) on a bounded sample of
     the step: the first `rows` rows of A with all of W, i.e. a rows x 4096 x
-    7168 slice of the same GEMM; TFLOP/s counts the sample's own FLOPs."""
+    7168 slice of the same GEMM (all 4096 rows when that fits the budget);
+    TFLOP/s counts the sample's own FLOPs."""
     from oracle import oracle as orc
     d, rows = _oracle_sample(orc, budget_s)
+    rows = M3 if rows >= M3 // 4 else rows
     t = time.perf_counter()
     _oracle_step(orc, d.a_bits[:rows], d.w_bits)
     dt = time.perf_counter() - t

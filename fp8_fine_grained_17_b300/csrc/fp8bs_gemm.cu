@@ -13,26 +13,38 @@
 // concerning the deepseek core readings", Figure 7(a)), so the promotion
 // interval here is one 128-wide K chunk.
 //
-// B300 design (not the pages' Hopper scheme): one persistent CTA per SM,
-// 384 threads, output tile 128 x 256.
-//   warp 0      TMA producer: A (128x128 B) and W (256x128 B) chunks into a
-//               4-stage shared-memory ring, 128-byte swizzled.
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4
-//               (K = 32 each) per chunk into one of two 256-column FP32 TMEM
-//               buffers, overwriting it (the chunk's partial P_kb).
+// B300 design (not the pages' Hopper scheme): persistent kernel, 384 threads
+// per CTA, one CTA per SM. Each CTA owns 128 output rows x kBN columns of a
+// tile (kBN = 128 or 256), and kCtas CTAs share one MMA:
+//   kCtas = 1  tile 128 x kBN; the CTA stages A (128 x 128 B) and W
+//              (kBN x 128 B) per chunk and issues its own MMAs.
+//   kCtas = 2  tile 256 x kBN computed by a CTA pair (cluster of 2) with
+//              tcgen05.mma.cta_group::2: each CTA stages its 128 A rows and
+//              half of the kBN W rows, the even CTA issues the MMA for both,
+//              and each CTA's TMEM gets the accumulator rows of its own A half.
+// The 512 TMEM columns hold 512 / kBN accumulator slots: with kBN = 128 four
+// chunks can be in flight between the tensor cores and the promotion warps,
+// which hides the MMA -> promotion -> MMA hand-off latency.
+// Warp roles (each CTA):
+//   warp 0      TMA producer: A and W chunks into a shared-memory ring of
+//               192 KB, 128-byte swizzled.
+//   warp 1      MMA issuer (one thread; only the even CTA of a pair): 4 x
+//               tcgen05.mma.kind::f8f6f4 (K = 32 each) per chunk into the
+//               next free TMEM slot, overwriting it (the chunk's partial
+//               P_kb).
 //   warp 2      TMEM allocator (512 columns).
-//   warp 3      scale loader: copies each chunk's 128 activation scales and
-//               two weight-block scales into an 8-slot shared-memory ring
-//               with cp.async (grouped GEMM: first builds the expert tile
-//               table), running up to 8 chunks ahead of the promotion warps.
-//   warps 4-11  promotion: each thread owns one row and 128 columns; per
-//               chunk it reads P_kb from TMEM (tcgen05.ld, the next 32
+//   warp 3      builds the expert tile table (a dense launch is one expert),
+//               then loads scales: each chunk's 128 activation scales and two
+//               weight-block scales into an 8-slot shared-memory ring with
+//               cp.async, running up to 8 chunks ahead of the promotion.
+//   warps 4-11  promotion: each thread owns one row and kBN/2 columns; per
+//               chunk it reads P_kb from TMEM (tcgen05.ld, the next 16
 //               columns in flight while the current ones are accumulated),
 //               frees the buffer, and accumulates acc += (sa * sw) * P_kb in
-//               FP32 registers. After the last chunk it converts and stores
-//               its row segment.
-// The two TMEM buffers let the tensor cores compute chunk kb+1 while the
-// promotion warps drain chunk kb.
+//               FP32 registers with the packed FMA pipe. After the last chunk
+//               it converts and stores its row segment.
+// The TMEM slots let the tensor cores compute the next chunks while the
+// promotion warps drain earlier ones.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -45,40 +57,53 @@
 namespace fp8bs {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 128;
-constexpr int kStages = 4;
+constexpr int BM = 128;   // output rows per CTA (TMEM lanes)
+constexpr int BK = 128;   // K chunk = one scale group
 constexpr int kScaleStages = 8;
-constexpr int kABytes = BM * BK;
-constexpr int kBBytes = BN * BK;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 384;
-constexpr int kTmemCols = 2 * BN;
+constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr int kProducerRegs = 56;
 constexpr int kEpilogueRegs = 224;
-constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, BN);
 
+template <int kCtas, int kBN>
+struct Cfg {
+    static constexpr int kBRows = kBN / kCtas;            // W rows staged per CTA
+    static constexpr int kABytes = BM * BK;
+    static constexpr int kBBytes = kBRows * BK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (192 * 1024) / kStageBytes;   // 4, 6 or 8
+    static constexpr int kSlots = kTmemCols / kBN;        // TMEM accumulator slots
+    static constexpr int kCols = kBN / 2;                 // columns per promotion thread
+    static constexpr int kTileRows = BM * kCtas;          // output rows per tile
+    static constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * kCtas, kBN);
+};
+
+template <int kCtas, int kBN>
 struct __align__(1024) Smem {
-    uint8_t a[kStages][kABytes];
-    uint8_t b[kStages][kBBytes];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tmem_full[2];
-    uint64_t tmem_empty[2];
+    using C = Cfg<kCtas, kBN>;
+    uint8_t a[C::kStages][C::kABytes];
+    uint8_t b[C::kStages][C::kBBytes];
+    uint64_t full[C::kStages];            // even CTA: both CTAs' TMA bytes
+    uint64_t empty[C::kStages];
+    uint64_t tmem_full[C::kSlots];
+    uint64_t tmem_empty[C::kSlots];       // even CTA: 8 arrivals per CTA of the pair
     uint64_t drain;
     uint64_t scale_full[kScaleStages];    // 32 cp.async arrivals (one per loader lane)
     uint64_t scale_empty[kScaleStages];   // 8 arrivals (one per promotion warp)
-    float scale_a[kScaleStages][BM];      // sa[m0 + r, kb]
-    float scale_w[kScaleStages][4];       // sw[e, n0/128 + h, kb], h = 0, 1
+    float scale_a[kScaleStages][BM];      // sa[row0 + r, kb]
+    float scale_w[kScaleStages][4];       // sw[e, (n0 + h kBN/2)/128, kb], h = 0, 1
     uint32_t tmem_base;
     int abort;
     int num_tiles;
-    int tile_start[kMaxExperts + 1];   // grouped: first tile index of each expert
-    int row_start[kMaxExperts + 1];    // grouped: copy of expert_offsets
+    int tile_start[kMaxExperts + 1];   // first tile index of each expert
+    int row_start[kMaxExperts + 1];    // copy of expert_offsets
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + alignment slack
+template <int kCtas, int kBN>
+constexpr size_t smem_bytes()
+{
+    return sizeof(Smem<kCtas, kBN>) + 1024;   // + alignment slack
+}
 
 struct Params {
     const float* sa;          // [rows, KB]
@@ -89,9 +114,9 @@ struct Params {
     int N;
     int KB;
     int NB;                   // N / 128
-    int n_tiles;              // ceil(N / 256)
+    int n_tiles;              // N / kBN
     int out_bf16;
-    const int32_t* offsets;   // grouped only
+    const int32_t* offsets;   // grouped only (nullptr: one expert, rows 0..M)
     int E;
     unsigned int* err;
 };
@@ -107,8 +132,10 @@ struct Tile {
 // Tile t of the launch: the expert e with tile_start[e] <= t < tile_start[e+1]
 // (binary search; a dense launch is one expert covering all rows), then the
 // m-tile and n-tile within that expert, m-tiles fastest.
-__device__ __forceinline__ Tile decode_tile(const Smem& sm, const Params& p, int t)
+template <int kCtas, int kBN>
+__device__ __forceinline__ Tile decode_tile(const Smem<kCtas, kBN>& sm, const Params& p, int t)
 {
+    constexpr int kTileRows = Cfg<kCtas, kBN>::kTileRows;
     int lo = 0, hi = p.E;   // invariant: tile_start[lo] <= t < tile_start[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -120,13 +147,13 @@ __device__ __forceinline__ Tile decode_tile(const Smem& sm, const Params& p, int
     const int e = lo;
     const int local = t - sm.tile_start[e];
     const int rows_e = sm.row_start[e + 1] - sm.row_start[e];
-    const int mt_e = (rows_e + BM - 1) / BM;
+    const int mt_e = (rows_e + kTileRows - 1) / kTileRows;
     const int mt = local % mt_e;
     const int nt = local / mt_e;
     Tile tile;
-    tile.m0 = sm.row_start[e] + static_cast<int64_t>(mt) * BM;
+    tile.m0 = sm.row_start[e] + static_cast<int64_t>(mt) * kTileRows;
     tile.row_end = sm.row_start[e + 1];
-    tile.n0 = nt * BN;
+    tile.n0 = nt * kBN;
     tile.expert = e;
     tile.b_row0 = e * p.N + tile.n0;
     return tile;
@@ -135,13 +162,16 @@ __device__ __forceinline__ Tile decode_tile(const Smem& sm, const Params& p, int
 // Warp 3: copy and validate expert_offsets (a dense launch uses {0, M}),
 // then build tile_start[] (exclusive prefix sum of m-tiles x n-tiles per
 // expert).
-__device__ void build_expert_table(Smem& sm, const Params& p, int lane)
+template <int kCtas, int kBN>
+__device__ void build_expert_table(Smem<kCtas, kBN>& sm, const Params& p, int lane)
 {
+    constexpr int kTileRows = Cfg<kCtas, kBN>::kTileRows;
     bool ok = true;
     for (int base = 0; base <= p.E; base += 32) {
         const int i = base + lane;
         if (i <= p.E)
-            sm.row_start[i] = p.offsets != nullptr ? p.offsets[i] : (i == 0 ? 0 : static_cast<int>(p.rows));
+            sm.row_start[i] =
+                p.offsets != nullptr ? p.offsets[i] : (i == 0 ? 0 : static_cast<int>(p.rows));
     }
     __syncwarp();
     int carry = 0;
@@ -153,7 +183,7 @@ __device__ void build_expert_table(Smem& sm, const Params& p, int lane)
             if (hi < lo)
                 ok = false;
             else
-                tiles = ((hi - lo + BM - 1) / BM) * p.n_tiles;
+                tiles = ((hi - lo + kTileRows - 1) / kTileRows) * p.n_tiles;
         }
         int incl = tiles;
 #pragma unroll
@@ -181,25 +211,34 @@ __device__ void build_expert_table(Smem& sm, const Params& p, int lane)
     }
 }
 
+template <int kCtas, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p)
 {
+    using C = Cfg<kCtas, kBN>;
+    using S = Smem<kCtas, kBN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
+    S& sm = *reinterpret_cast<S*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Position in the CTA pair (always 0 for kCtas = 1); tiles are handed out
+    // per pair.
+    const uint32_t rank = kCtas == 2 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int first_tile = static_cast<int>(blockIdx.x) / kCtas;
+    const int tile_step = static_cast<int>(gridDim.x) / kCtas;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&sm.full[s]), 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kSlots; ++b) {
             mbar_init(smem_addr(&sm.tmem_full[b]), 1);
-            mbar_init(smem_addr(&sm.tmem_empty[b]), 8);   // one arrive per promotion warp
+            mbar_init(smem_addr(&sm.tmem_empty[b]), 8 * kCtas);   // one per promotion warp
         }
         mbar_init(smem_addr(&sm.drain), 1);
         for (int s = 0; s < kScaleStages; ++s) {
@@ -214,13 +253,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         tma_prefetch_desc(&map_b);
     }
     if (warp == 2) {
-        tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<kCtas>(smem_addr(&sm.tmem_base), kTmemCols);
+        tmem_relinquish<kCtas>();
     }
     if (warp == 3)
         build_expert_table(sm, p, lane);
     tc_fence_before();
     __syncthreads();
+    if (kCtas == 2)
+        cluster_sync_all();   // both CTAs' barriers exist before any remote use
     tc_fence_after();
 
     const uint32_t tmem_base = sm.tmem_base;
@@ -229,77 +270,129 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     if (warp < 4) {
         regs_dec<kProducerRegs>();
-        if (warp == 0 && lane == 0) {
+        if (warp == 0) {
             // ---------------------------------------------------- TMA producer
+            // The whole warp runs the loop; one elected lane issues the copies.
             uint32_t chunk = 0;
+            uint32_t s = 0, ph = 0;   // stage and its phase parity
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
                 const Tile tile = decode_tile(sm, p, t);
+                const int32_t a_row = static_cast<int32_t>(tile.m0) + static_cast<int32_t>(rank) * BM;
+                const int32_t b_row = tile.b_row0 + static_cast<int32_t>(rank) * C::kBRows;
                 for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                    const uint32_t s = chunk % kStages;
-                    const uint32_t ph = (chunk / kStages) & 1u;
-                    if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err)) {
+                    const bool ready = mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err);
+                    if (!__all_sync(0xFFFFFFFFu, ready)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = smem_addr(&sm.full[s]);
-                    mbar_arrive_expect_tx(full, kStageBytes);
-                    tma_load_2d(smem_addr(sm.a[s]), &map_a, full, kb * BK, static_cast<int32_t>(tile.m0));
-                    tma_load_2d(smem_addr(sm.b[s]), &map_b, full, kb * BK, tile.b_row0);
+                    if (elect_one()) {
+                        if (kCtas == 1) {
+                            mbar_arrive_expect_tx(full, C::kStageBytes);
+                            tma_load_2d(smem_addr(sm.a[s]), &map_a, full, kb * BK, a_row);
+                            tma_load_2d(smem_addr(sm.b[s]), &map_b, full, kb * BK, b_row);
+                        } else {
+                            // Both CTAs' copies complete on the even CTA's barrier.
+                            if (leader)
+                                mbar_arrive_expect_tx(full, 2 * C::kStageBytes);
+                            const uint32_t full0 = map_to_cta(full, 0);
+                            tma_load_2d_pair(smem_addr(sm.a[s]), &map_a, full0, kb * BK, a_row);
+                            tma_load_2d_pair(smem_addr(sm.b[s]), &map_b, full0, kb * BK, b_row);
+                        }
+                    }
+                    __syncwarp();
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (!ok) {
                 // Let the copies already issued land before the CTA exits.
-                const uint32_t first = chunk > kStages ? chunk - kStages : 0;
-                for (uint32_t c = first; c < chunk; ++c)
-                    mbar_wait_drain(smem_addr(&sm.full[c % kStages]), (c / kStages) & 1u,
-                                    kWaitLimitNs, p.err);
-            }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------ MMA issuer
-            uint32_t chunk = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                    const uint32_t s = chunk % kStages;
-                    const uint32_t ph = (chunk / kStages) & 1u;
-                    const uint32_t b = chunk & 1u;
-                    const uint32_t tph = (chunk >> 1) & 1u;
-                    if (!mbar_wait(smem_addr(&sm.tmem_empty[b]), tph ^ 1u, abort_flag, p.err) ||
-                        !mbar_wait(smem_addr(&sm.full[s]), ph, abort_flag, p.err)) {
-                        ok = false;
-                        break;
+                if (kCtas == 1 || leader) {
+                    const uint32_t first = chunk > C::kStages ? chunk - C::kStages : 0;
+                    for (uint32_t c = first; c < chunk; ++c)
+                        mbar_wait_drain(smem_addr(&sm.full[c % C::kStages]),
+                                        (c / C::kStages) & 1u, kWaitLimitNs, p.err);
+                } else {
+                    // The odd CTA's copies complete on its partner's barrier,
+                    // which it cannot wait on: give them a fixed time.
+                    const unsigned long long t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) {
                     }
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + b * BN;
-                    const uint32_t a_addr = smem_addr(sm.a[s]);
-                    const uint32_t b_addr = smem_addr(sm.b[s]);
-#pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_e4m3(d, smem_desc_k_sw128(a_addr + 32 * k),
-                                 smem_desc_k_sw128(b_addr + 32 * k), kIdesc, k > 0 ? 1u : 0u);
-                    mma_commit(smem_addr(&sm.empty[s]));
-                    mma_commit(smem_addr(&sm.tmem_full[b]));
                 }
             }
-            // All MMAs issued by this thread complete before TMEM is released.
-            mma_commit(smem_addr(&sm.drain));
-            mbar_wait_drain(smem_addr(&sm.drain), 0, kWaitLimitNs, p.err);
+        } else if (warp == 1 && leader) {
+            // ------------------------------------------------------ MMA issuer
+            // The whole warp runs the loop with warp-uniform values; one
+            // elected lane issues each chunk's MMAs and commits (the same
+            // lane every time: the warp is converged and fully active).
+            uint32_t s = 0, ph = 0;   // smem stage and its phase parity
+            uint32_t b = 0, tph = 0;  // TMEM slot and its phase parity
+            bool ok = true;
+            // Descriptors of stage 0; stage s / K step k add their byte offset
+            // >> 4 to the start-address field (shared addresses < 256 KB).
+            const uint64_t adesc0 = smem_desc_k_sw128(smem_addr(sm.a[0]));
+            const uint64_t bdesc0 = smem_desc_k_sw128(smem_addr(sm.b[0]));
+            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    const uint32_t empty_bar = smem_addr(&sm.tmem_empty[b]);
+                    const uint32_t full_bar = smem_addr(&sm.full[s]);
+                    // Both conditions are usually met already: test them
+                    // together, wait only if one is not.
+                    bool ready = mbar_test_wait(empty_bar, tph ^ 1u) & mbar_test_wait(full_bar, ph);
+                    if (!__all_sync(0xFFFFFFFFu, ready)) {
+                        ready = mbar_wait(empty_bar, tph ^ 1u, abort_flag, p.err) &&
+                                mbar_wait(full_bar, ph, abort_flag, p.err);
+                        if (!__all_sync(0xFFFFFFFFu, ready)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        const uint32_t d = tmem_base + b * kBN;
+                        const uint64_t ad = adesc0 + ((s * C::kABytes) >> 4);
+                        const uint64_t bd = bdesc0 + ((s * C::kBBytes) >> 4);
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)
+                            mma_e4m3<kCtas>(d, ad + 2 * k, bd + 2 * k, C::kIdesc, k > 0 ? 1u : 0u);
+                        mma_commit<kCtas>(smem_addr(&sm.empty[s]));
+                        mma_commit<kCtas>(smem_addr(&sm.tmem_full[b]));
+                    }
+                    __syncwarp();
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++b == C::kSlots) {
+                        b = 0;
+                        tph ^= 1u;
+                    }
+                }
+            }
+            // All MMAs issued by this warp complete before TMEM is released.
+            if (elect_one()) {
+                mma_commit<kCtas>(smem_addr(&sm.drain));
+                mbar_wait_drain(smem_addr(&sm.drain), 0, kWaitLimitNs, p.err);
+            }
+            __syncwarp();
         } else if (warp == 3) {
             // ---------------------------------------------------- scale loader
             uint32_t chunk = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
                 const Tile tile = decode_tile(sm, p, t);
                 // Rows past the tile's end read a valid row; their products
                 // are never stored.
                 const float* src_a[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int64_t row = tile.m0 + lane + 32 * i;
+                    const int64_t row = tile.m0 + rank * BM + lane + 32 * i;
                     src_a[i] = p.sa + (row < p.rows ? row : p.rows - 1) * p.KB;
                 }
-                const int nbh = min(tile.n0 / 128 + (lane & 1), p.NB - 1);
+                const int nbh = min((tile.n0 + (lane & 1) * C::kCols) / 128, p.NB - 1);
                 const float* src_w = p.sw + (static_cast<int64_t>(tile.expert) * p.NB + nbh) * p.KB;
                 for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
                     const uint32_t s = chunk % kScaleStages;
@@ -324,104 +417,212 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         regs_inc<kEpilogueRegs>();
         // ------------------------------------------------------- promotion
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 4) >> 2;      // output columns 128*half .. +127
+        const int half = (warp - 4) >> 2;      // output columns kCols*half .. +kCols-1
         const int r = quarter * 32 + lane;
+        // The slot-free arrivals of both CTAs of a pair go to the even CTA
+        // (tmem_empty[b] is at tmem_empty[0] + 8 b bytes).
+        const uint32_t tmem_empty0 = kCtas == 1 ? smem_addr(&sm.tmem_empty[0])
+                                                : map_to_cta(smem_addr(&sm.tmem_empty[0]), 0);
         uint32_t chunk = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile tile = decode_tile(sm, p, t);
-            const int64_t row = tile.m0 + r;
-            const int n_col = tile.n0 + half * 128;
-            const bool live = row < tile.row_end && n_col < p.N;
-
-            // 128 FP32 accumulators as 64 pairs for the packed FMA pipe.
-            float2 acc[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                acc[i] = make_float2(0.0f, 0.0f);
-#pragma unroll 1
-            for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                const uint32_t ss = chunk % kScaleStages;
-                const uint32_t sph = (chunk / kScaleStages) & 1u;
-                const uint32_t b = chunk & 1u;
-                const uint32_t tph = (chunk >> 1) & 1u;
-                // The warp continues only if every lane saw the phases
-                // complete: the TMEM loads below are warp-collective.
-                bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), sph, abort_flag, p.err);
-                float scale = 0.0f;
-                if (ready)
-                    scale = sm.scale_a[ss][r] * sm.scale_w[ss][half];
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_addr(&sm.scale_empty[ss]));
-                ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), tph, abort_flag, p.err);
-                if (!__all_sync(0xFFFFFFFFu, ready)) {
-                    ok = false;
-                    break;
-                }
+        // Scale of chunk c: sa[row, kb] * sw[n-block, kb] from the scale ring;
+        // the slot goes back to the loader right after the read.
+        auto take_scale = [&](uint32_t c, float& scale) -> bool {
+            const uint32_t ss = c % kScaleStages;
+            const bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), (c / kScaleStages) & 1u,
+                                         abort_flag, p.err);
+            scale = ready ? sm.scale_a[ss][r] * sm.scale_w[ss][half] : 0.0f;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&sm.scale_empty[ss]));
+            return ready;
+        };
+        auto give_slot = [&](uint32_t c) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (kCtas == 1)
+                    mbar_arrive(tmem_empty0 + 8 * (c % C::kSlots));
+                else
+                    mbar_arrive_remote(tmem_empty0 + 8 * (c % C::kSlots));
+            }
+        };
+        if constexpr (C::kCols == 64) {
+            // Each chunk: both 32-column loads in flight at once, one wait,
+            // the slot goes back, then the arithmetic.
+            // acquire: scale and TMEM load (issued, not waited) of chunk c.
+            auto acquire = [&](uint32_t c, uint32_t (&x0)[32], uint32_t (&x1)[32], float& scale) -> bool {
+                bool ready = take_scale(c, scale);
+                const uint32_t b = c % C::kSlots;
+                ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), (c / C::kSlots) & 1u,
+                                           abort_flag, p.err);
+                if (!__all_sync(0xFFFFFFFFu, ready))
+                    return false;
                 tc_fence_after();
                 const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + half * 128;
-                const float2 scale2 = make_float2(scale, scale);
-                // Column blocks 0..3 of 32: the load of block j+1 is in flight
-                // while block j is accumulated.
-                uint32_t va[32], vb[32];
-                tmem_ld_32x32b_x32(taddr, va);
-                tmem_ld_wait(va);
-                tmem_ld_32x32b_x32(taddr + 32, vb);
+                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * C::kCols;
+                tmem_ld_32x32b_x32(taddr, x0);
+                tmem_ld_32x32b_x32(taddr + 32, x1);
+                return true;
+            };
+            auto complete = [&](uint32_t c, uint32_t (&x0)[32], uint32_t (&x1)[32]) {
+                tmem_ld_wait(x0);
+                tmem_ld_tie(x1);
+                give_slot(c);
+            };
+            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
+                const Tile tile = decode_tile(sm, p, t);
+                const int64_t row = tile.m0 + rank * BM + r;
+                const int n_col = tile.n0 + half * C::kCols;
+                const bool live = row < tile.row_end && n_col < p.N;
+                float2 acc[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[0 + i] = __ffma2_rn(
-                        make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])),
-                        scale2, acc[0 + i]);
-                tmem_ld_wait(vb);
-                tmem_ld_32x32b_x32(taddr + 64, va);
+                for (int i = 0; i < 32; ++i)
+                    acc[i] = make_float2(0.0f, 0.0f);
+                auto accumulate = [&](uint32_t (&x0)[32], uint32_t (&x1)[32], float scale) {
+                    const float2 scale2 = make_float2(scale, scale);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[16 + i] = __ffma2_rn(
-                        make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])),
-                        scale2, acc[16 + i]);
-                tmem_ld_wait(va);
-                tmem_ld_32x32b_x32(taddr + 96, vb);
+                    for (int i = 0; i < 16; ++i)
+                        acc[i] = __ffma2_rn(
+                            make_float2(__uint_as_float(x0[2 * i]), __uint_as_float(x0[2 * i + 1])),
+                            scale2, acc[i]);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[32 + i] = __ffma2_rn(
-                        make_float2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])),
-                        scale2, acc[32 + i]);
-                tmem_ld_wait(vb);
-                // Every TMEM read of this buffer is complete: hand it back.
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_addr(&sm.tmem_empty[b]));
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    acc[48 + i] = __ffma2_rn(
-                        make_float2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])),
-                        scale2, acc[48 + i]);
-            }
-            if (ok && live) {
-                if (p.out_bf16) {
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + row * p.ldc + n_col;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        uint4 pk;
-                        __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
-                        __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
-                        __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
-                        __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
-                        memcpy(&pk.x, &h0, 4);
-                        memcpy(&pk.y, &h1, 4);
-                        memcpy(&pk.z, &h2, 4);
-                        memcpy(&pk.w, &h3, 4);
-                        reinterpret_cast<uint4*>(dst)[i] = pk;
+                    for (int i = 0; i < 16; ++i)
+                        acc[16 + i] = __ffma2_rn(
+                            make_float2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1])),
+                            scale2, acc[16 + i]);
+                };
+#pragma unroll 1
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    uint32_t x0[32], x1[32];
+                    float scale;
+                    if (!acquire(chunk + kb, x0, x1, scale)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
+                    complete(chunk + kb, x0, x1);
+                    accumulate(x0, x1, scale);
+                }
+                chunk += p.KB;
+                if (!ok)
+                    break;
+                if (ok && live) {
+                    if (p.out_bf16) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + row * p.ldc + n_col;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        reinterpret_cast<float4*>(dst)[i] = make_float4(
-                            acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+                        for (int i = 0; i < C::kCols / 8; ++i) {
+                            uint4 pk;
+                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
+                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
+                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
+                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
+                            memcpy(&pk.x, &h0, 4);
+                            memcpy(&pk.y, &h1, 4);
+                            memcpy(&pk.z, &h2, 4);
+                            memcpy(&pk.w, &h3, 4);
+                            reinterpret_cast<uint4*>(dst)[i] = pk;
+                        }
+                    } else {
+                        float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
+#pragma unroll
+                        for (int i = 0; i < C::kCols / 4; ++i)
+                            reinterpret_cast<float4*>(dst)[i] = make_float4(
+                                acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+                    }
+                }
+            }
+        } else {
+            uint32_t chunk = 0;
+            bool ok = true;
+            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
+                const Tile tile = decode_tile(sm, p, t);
+                const int64_t row = tile.m0 + rank * BM + r;
+                const int n_col = tile.n0 + half * C::kCols;
+                const bool live = row < tile.row_end && n_col < p.N;
+
+                // kCols FP32 accumulators as pairs for the packed FMA pipe.
+                float2 acc[C::kCols / 2];
+#pragma unroll
+                for (int i = 0; i < C::kCols / 2; ++i)
+                    acc[i] = make_float2(0.0f, 0.0f);
+    #pragma unroll 1
+                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
+                    const uint32_t ss = chunk % kScaleStages;
+                    const uint32_t sph = (chunk / kScaleStages) & 1u;
+                    const uint32_t b = chunk % C::kSlots;
+                    const uint32_t tph = (chunk / C::kSlots) & 1u;
+                    // The warp continues only if every lane saw the phases
+                    // complete: the TMEM loads below are warp-collective.
+                    bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), sph, abort_flag, p.err);
+                    float scale = 0.0f;
+                    if (ready)
+                        scale = sm.scale_a[ss][r] * sm.scale_w[ss][half];
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_addr(&sm.scale_empty[ss]));
+                    ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), tph, abort_flag, p.err);
+                    if (!__all_sync(0xFFFFFFFFu, ready)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t taddr =
+                        tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * C::kCols;
+                    const float2 scale2 = make_float2(scale, scale);
+                    // Column blocks j of 16: the load of block j+1 is in flight
+                    // while block j is accumulated.
+                    constexpr int kBlocks = C::kCols / 16;
+                    uint32_t v[2][16];
+                    tmem_ld_32x32b_x16(taddr, v[0]);
+                    tmem_ld_wait(v[0]);
+#pragma unroll
+                    for (int j = 0; j < kBlocks; ++j) {
+                        if (j + 1 < kBlocks)
+                            tmem_ld_32x32b_x16(taddr + 16 * (j + 1), v[(j + 1) & 1]);
+                        else {
+                            // Every TMEM read of this buffer has been issued and
+                            // waited for: hand it back.
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (kCtas == 1)
+                                    mbar_arrive(tmem_empty0 + 8 * b);
+                                else
+                                    mbar_arrive_remote(tmem_empty0 + 8 * b);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc[8 * j + i] = __ffma2_rn(make_float2(__uint_as_float(v[j & 1][2 * i]),
+                                                                    __uint_as_float(v[j & 1][2 * i + 1])),
+                                                        scale2, acc[8 * j + i]);
+                        if (j + 1 < kBlocks)
+                            tmem_ld_wait(v[(j + 1) & 1]);
+                    }
+                }
+                if (ok && live) {
+                    if (p.out_bf16) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + row * p.ldc + n_col;
+#pragma unroll
+                        for (int i = 0; i < C::kCols / 8; ++i) {
+                            uint4 pk;
+                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
+                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
+                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
+                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
+                            memcpy(&pk.x, &h0, 4);
+                            memcpy(&pk.y, &h1, 4);
+                            memcpy(&pk.z, &h2, 4);
+                            memcpy(&pk.w, &h3, 4);
+                            reinterpret_cast<uint4*>(dst)[i] = pk;
+                        }
+                    } else {
+                        float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
+#pragma unroll
+                        for (int i = 0; i < C::kCols / 4; ++i)
+                            reinterpret_cast<float4*>(dst)[i] = make_float4(
+                                acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+                    }
                 }
             }
         }
@@ -429,9 +630,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
+    if (kCtas == 2)
+        cluster_sync_all();   // no remote arrival or MMA operand read is left in flight
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc<kCtas>(tmem_base, kTmemCols);
     }
 }
 
@@ -471,27 +674,59 @@ bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
     return r == CUDA_SUCCESS;
 }
 
-fp8bs_status configure_once(int device)
+// Per device and shape: the dynamic shared-memory opt-in and the number of
+// work units (CTAs, or CTA pairs, which must share a GPC) resident at once.
+template <int kCtas, int kBN>
+fp8bs_status configure_once(int device, int sm_count, int* max_units)
 {
     static std::mutex mu;
-    static bool done[64] = {};
+    static int units[64] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64)
         return FP8BS_ERR_CUDA;
-    if (!done[device]) {
-        if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes)) != cudaSuccess) {
+    if (units[device] == 0) {
+        const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
+        const size_t smem = smem_bytes<kCtas, kBN>();
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess) {
             cudaGetLastError();
             return FP8BS_ERR_CUDA;
         }
-        done[device] = true;
+        int n = sm_count;
+        if (kCtas == 2) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (sm_count / 2));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess ||
+                clusters <= 0) {
+                cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            n = clusters;
+        }
+        units[device] = n;
     }
+    *max_units = units[device];
     return FP8BS_OK;
 }
 
+// rows: rows of A; w_rows: rows of the stacked W. The number of tiles is
+// computed on the device from the expert table; the grid is the resident
+// maximum, capped by an upper bound of the tiles.
+template <int kCtas, int kBN>
 fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
-                    int64_t K, int64_t tile_bound, cudaStream_t stream)
+                    int64_t K, cudaStream_t stream)
 {
+    using C = Cfg<kCtas, kBN>;
     DeviceInfo info;
     fp8bs_status st = require_sm103(&info);
     if (st != FP8BS_OK)
@@ -499,21 +734,47 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     p.err = device_error_word();
     if (p.err == nullptr)
         return FP8BS_ERR_CUDA;
+    p.n_tiles = p.N / kBN;
+    const int64_t tile_bound = (rows / C::kTileRows + p.E) * static_cast<int64_t>(p.n_tiles);
+    if (tile_bound > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
     CUtensorMap map_a, map_b;
     memset(&map_a, 0, sizeof map_a);
     memset(&map_b, 0, sizeof map_b);
     if (K > 0) {
-        if (!encode_operand(&map_a, qa, rows, K, BM) || !encode_operand(&map_b, qw, w_rows, K, BN))
+        if (!encode_operand(&map_a, qa, rows, K, BM) ||
+            !encode_operand(&map_b, qw, w_rows, K, C::kBRows))
             return FP8BS_ERR_CUDA;
     }
-    st = configure_once(info.device);
+    int max_units = 0;
+    st = configure_once<kCtas, kBN>(info.device, info.sm_count, &max_units);
     if (st != FP8BS_OK)
         return st;
-    const int grid = static_cast<int>(tile_bound < info.sm_count ? tile_bound : info.sm_count);
-    if (grid <= 0)
+    const int units = static_cast<int>(tile_bound < max_units ? tile_bound : max_units);
+    if (units <= 0)
         return FP8BS_OK;
-    fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, p);
-    return launch_status();
+    const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
+    if (kCtas == 1) {
+        kernel<<<units, kThreads, smem_bytes<kCtas, kBN>(), stream>>>(map_a, map_b, p);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<kCtas, kBN>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
 }
 
 fp8bs_status check_common(const void* qa, const float* sa, const void* qw, const float* sw,
@@ -536,56 +797,108 @@ fp8bs_status check_common(const void* qa, const float* sa, const void* qw, const
     return FP8BS_OK;
 }
 
-}  // namespace
-}  // namespace fp8bs
-
-using namespace fp8bs;
-
-extern "C" fp8bs_status fp8bs_gemm(const uint8_t* qa, const float* sa, const uint8_t* qw,
-                                   const float* sw, void* c, fp8bs_out_dtype out_dtype, int64_t M,
-                                   int64_t N, int64_t K, int64_t ldc, fp8bs_stream_t stream)
+Params make_params(const float* sa, const float* sw, void* c, fp8bs_out_dtype out_dtype,
+                   int64_t rows, int64_t N, int64_t K, int64_t ldc, const int32_t* offsets, int E)
 {
-    if (M < 0 || N < 0 || K < 0)
-        return FP8BS_ERR_INVALID_ARG;
-    if (K % BK != 0 || N % 128 != 0)
-        return FP8BS_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0)
-        return FP8BS_OK;
-    fp8bs_status st = check_common(qa, sa, qw, sw, c, out_dtype, N, K, ldc);
-    if (st != FP8BS_OK)
-        return st;
-    const int64_t m_tiles = (M + BM - 1) / BM;
-    const int64_t n_tiles = (N + BN - 1) / BN;
-    if (M > 0x7FFFFFFF || m_tiles * n_tiles > 0x7FFFFFFF)
-        return FP8BS_ERR_UNSUPPORTED;
-
     Params p{};
     p.sa = sa;
     p.sw = sw;
     p.c = c;
     p.ldc = ldc;
-    p.rows = M;
+    p.rows = rows;
     p.N = static_cast<int>(N);
     p.KB = static_cast<int>(K / BK);
     p.NB = static_cast<int>(N / 128);
-    p.n_tiles = static_cast<int>(n_tiles);
     p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
-    p.offsets = nullptr;
-    p.E = 1;
-    return launch(qa, M, qw, N, p, K, m_tiles * n_tiles,
-                         reinterpret_cast<cudaStream_t>(stream));
+    p.offsets = offsets;
+    p.E = E;
+    return p;
 }
 
-extern "C" fp8bs_status fp8bs_grouped_gemm(const uint8_t* qa, const float* sa,
-                                           const int32_t* expert_offsets, int32_t E,
-                                           int64_t total_M, const uint8_t* qw, const float* sw,
-                                           void* c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
-                                           int64_t ldc, fp8bs_stream_t stream)
+// Tile shape of a launch (fp8bs_tile without AUTO): CTAs per MMA and tile
+// width. Single CTA, 128 x 256 tiles is the automatic choice: on B300 it is
+// the fastest or within run-to-run noise of the fastest shape across the
+// dense and MoE workloads, and it needs no cluster co-scheduling. A 256-wide
+// tile needs N % 256 == 0 to be fully used; other N take 128-wide tiles.
+fp8bs_tile auto_tile(int64_t N)
+{
+    return N % 256 == 0 ? FP8BS_TILE_128x256 : FP8BS_TILE_128x128;
+}
+
+fp8bs_status launch_tile(fp8bs_tile tile, const uint8_t* qa, int64_t rows, const uint8_t* qw,
+                         int64_t w_rows, const Params& p, int64_t K, cudaStream_t s)
+{
+    switch (tile) {
+    case FP8BS_TILE_128x256: return launch<1, 256>(qa, rows, qw, w_rows, p, K, s);
+    case FP8BS_TILE_128x128: return launch<1, 128>(qa, rows, qw, w_rows, p, K, s);
+    case FP8BS_TILE_PAIR_256x256: return launch<2, 256>(qa, rows, qw, w_rows, p, K, s);
+    case FP8BS_TILE_PAIR_256x128: return launch<2, 128>(qa, rows, qw, w_rows, p, K, s);
+    default: break;
+    }
+    return FP8BS_ERR_INVALID_ARG;
+}
+
+bool valid_tile(fp8bs_tile tile, int64_t N)
+{
+    switch (tile) {
+    case FP8BS_TILE_AUTO:
+    case FP8BS_TILE_128x256:
+    case FP8BS_TILE_128x128:
+    case FP8BS_TILE_PAIR_256x128: return true;
+    case FP8BS_TILE_PAIR_256x256: return N % 256 == 0;   // the pair splits W tiles in halves
+    }
+    return false;
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" fp8bs_status fp8bs_gemm_tiled(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                         const float* sw, void* c, fp8bs_out_dtype out_dtype,
+                                         int64_t M, int64_t N, int64_t K, int64_t ldc,
+                                         fp8bs_tile tile, fp8bs_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % BK != 0 || N % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    if (!valid_tile(tile, N))
+        return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    fp8bs_status st = check_common(qa, sa, qw, sw, c, out_dtype, N, K, ldc);
+    if (st != FP8BS_OK)
+        return st;
+    if (M > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
+    const Params p = make_params(sa, sw, c, out_dtype, M, N, K, ldc, nullptr, 1);
+    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N) : tile, qa, M, qw, N, p, K,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8bs_status fp8bs_gemm(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                   const float* sw, void* c, fp8bs_out_dtype out_dtype, int64_t M,
+                                   int64_t N, int64_t K, int64_t ldc, fp8bs_stream_t stream)
+{
+    return fp8bs_gemm_tiled(qa, sa, qw, sw, c, out_dtype, M, N, K, ldc, FP8BS_TILE_AUTO, stream);
+}
+
+extern "C" fp8bs_status fp8bs_grouped_gemm_tiled(const uint8_t* qa, const float* sa,
+                                                 const int32_t* expert_offsets, int32_t E,
+                                                 int64_t total_M, const uint8_t* qw,
+                                                 const float* sw, void* c,
+                                                 fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
+                                                 int64_t ldc, fp8bs_tile tile,
+                                                 fp8bs_stream_t stream)
 {
     if (E < 1 || total_M < 0 || N < 0 || K < 0)
         return FP8BS_ERR_INVALID_ARG;
     if (E > kMaxExperts || K % BK != 0 || N % 128 != 0)
         return FP8BS_ERR_UNSUPPORTED;
+    if (!valid_tile(tile, N))
+        return FP8BS_ERR_INVALID_ARG;
     if (total_M == 0 || N == 0)
         return FP8BS_OK;
     if (expert_offsets == nullptr || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
@@ -595,24 +908,17 @@ extern "C" fp8bs_status fp8bs_grouped_gemm(const uint8_t* qa, const float* sa,
         return st;
     if (total_M > 0x7FFFFFFF || static_cast<int64_t>(E) * N > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
-    const int64_t n_tiles = (N + BN - 1) / BN;
-    const int64_t tile_bound = (total_M / BM + E) * n_tiles;
-    if (tile_bound > 0x7FFFFFFF)
-        return FP8BS_ERR_UNSUPPORTED;
+    const Params p = make_params(sa, sw, c, out_dtype, total_M, N, K, ldc, expert_offsets, E);
+    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N) : tile, qa, total_M, qw,
+                       static_cast<int64_t>(E) * N, p, K, reinterpret_cast<cudaStream_t>(stream));
+}
 
-    Params p{};
-    p.sa = sa;
-    p.sw = sw;
-    p.c = c;
-    p.ldc = ldc;
-    p.rows = total_M;
-    p.N = static_cast<int>(N);
-    p.KB = static_cast<int>(K / BK);
-    p.NB = static_cast<int>(N / 128);
-    p.n_tiles = static_cast<int>(n_tiles);
-    p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
-    p.offsets = expert_offsets;
-    p.E = E;
-    return launch(qa, total_M, qw, static_cast<int64_t>(E) * N, p, K, tile_bound,
-                        reinterpret_cast<cudaStream_t>(stream));
+extern "C" fp8bs_status fp8bs_grouped_gemm(const uint8_t* qa, const float* sa,
+                                           const int32_t* expert_offsets, int32_t E,
+                                           int64_t total_M, const uint8_t* qw, const float* sw,
+                                           void* c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
+                                           int64_t ldc, fp8bs_stream_t stream)
+{
+    return fp8bs_grouped_gemm_tiled(qa, sa, expert_offsets, E, total_M, qw, sw, c, out_dtype, N, K,
+                                    ldc, FP8BS_TILE_AUTO, stream);
 }

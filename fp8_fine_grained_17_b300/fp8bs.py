@@ -20,6 +20,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8bs.h")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 OUT_F32, OUT_BF16 = 0, 1
+TILE_AUTO, TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128 = 0, 1, 2, 3, 4
+TILES = (TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128)
 
 
 class Fp8bsError(RuntimeError):
@@ -50,6 +52,12 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_grouped_gemm.argtypes = [vp, f32p, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
                                          i64, i64, i64, vp]
         L.fp8bs_grouped_gemm.restype = st
+        L.fp8bs_gemm_tiled.argtypes = [vp, f32p, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64,
+                                       ctypes.c_int, vp]
+        L.fp8bs_gemm_tiled.restype = st
+        L.fp8bs_grouped_gemm_tiled.argtypes = [vp, f32p, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
+                                               i64, i64, i64, ctypes.c_int, vp]
+        L.fp8bs_grouped_gemm_tiled.restype = st
         L.fp8bs_status_string.argtypes = [ctypes.c_int]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
@@ -126,27 +134,35 @@ def _out_dtype(c: torch.Tensor) -> int:
     raise ValueError("output must be float32 or bfloat16")
 
 
-def fp8bs_gemm(qa, sa, qw, sw, c, stream=None):
-    """C[M, N] = dequant(qa, sa) @ dequant(qw, sw)^T into c (fp32 or bf16)."""
+def fp8bs_gemm(qa, sa, qw, sw, c, stream=None, tile=TILE_AUTO):
+    """C[M, N] = dequant(qa, sa) @ dequant(qw, sw)^T into c (fp32 or bf16).
+    A tile other than TILE_AUTO goes through fp8bs_gemm_tiled."""
     M, K = qa.shape
     N = qw.shape[0]
     for t in (qa, sa, qw, sw):
         assert t.is_contiguous()
-    _check("fp8bs_gemm", lib().fp8bs_gemm(
-        _ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw), _ptr(c), _out_dtype(c),
-        M, N, K, _row_stride(c), _stream(stream)))
+    args = (_ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw), _ptr(c), _out_dtype(c),
+            M, N, K, _row_stride(c))
+    if tile == TILE_AUTO:
+        _check("fp8bs_gemm", lib().fp8bs_gemm(*args, _stream(stream)))
+    else:
+        _check("fp8bs_gemm_tiled", lib().fp8bs_gemm_tiled(*args, int(tile), _stream(stream)))
 
 
-def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None):
+def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None, tile=TILE_AUTO):
     """Per expert e: rows offsets[e]:offsets[e+1] of A times W_e^T."""
     total_M, K = qa.shape
     E, N, _ = qw.shape
     assert expert_offsets.dtype == torch.int32 and expert_offsets.numel() == E + 1
     for t in (qa, sa, qw, sw, expert_offsets):
         assert t.is_contiguous()
-    _check("fp8bs_grouped_gemm", lib().fp8bs_grouped_gemm(
-        _ptr(_u8(qa)), _ptr(sa), _ptr(expert_offsets), E, total_M, _ptr(_u8(qw)), _ptr(sw),
-        _ptr(c), _out_dtype(c), N, K, _row_stride(c), _stream(stream)))
+    args = (_ptr(_u8(qa)), _ptr(sa), _ptr(expert_offsets), E, total_M, _ptr(_u8(qw)), _ptr(sw),
+            _ptr(c), _out_dtype(c), N, K, _row_stride(c))
+    if tile == TILE_AUTO:
+        _check("fp8bs_grouped_gemm", lib().fp8bs_grouped_gemm(*args, _stream(stream)))
+    else:
+        _check("fp8bs_grouped_gemm_tiled",
+               lib().fp8bs_grouped_gemm_tiled(*args, int(tile), _stream(stream)))
 
 
 def fp8bs_last_device_error(stream=None) -> int:
@@ -172,13 +188,14 @@ def quantize_weight(w: torch.Tensor, stream=None):
     return q, s
 
 
-def gemm(qa, sa, qw, sw, out_dtype=torch.bfloat16, stream=None):
+def gemm(qa, sa, qw, sw, out_dtype=torch.bfloat16, stream=None, tile=TILE_AUTO):
     c = torch.empty((qa.shape[0], qw.shape[0]), dtype=out_dtype, device=qa.device)
-    fp8bs_gemm(qa, sa, qw, sw, c, stream)
+    fp8bs_gemm(qa, sa, qw, sw, c, stream, tile)
     return c
 
 
-def grouped_gemm(qa, sa, expert_offsets, qw, sw, out_dtype=torch.bfloat16, stream=None):
+def grouped_gemm(qa, sa, expert_offsets, qw, sw, out_dtype=torch.bfloat16, stream=None,
+                 tile=TILE_AUTO):
     c = torch.zeros((qa.shape[0], qw.shape[1]), dtype=out_dtype, device=qa.device)
-    fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream)
+    fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream, tile)
     return c

@@ -66,6 +66,20 @@ typedef enum {
 typedef enum { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 } fp8bs_out_dtype;
 
 /*
+ * Output tile of the GEMM kernels (all give identical results; they differ
+ * only in speed). AUTO picks 128x256 when N % 256 == 0, else 128x128. The
+ * PAIR shapes run a CTA pair (thread-block cluster of 2) per tile with the
+ * pair-wide tensor-core MMA; PAIR_256x256 needs N % 256 == 0.
+ */
+typedef enum {
+    FP8BS_TILE_AUTO = 0,
+    FP8BS_TILE_128x256 = 1,
+    FP8BS_TILE_128x128 = 2,
+    FP8BS_TILE_PAIR_256x256 = 3,
+    FP8BS_TILE_PAIR_256x128 = 4
+} fp8bs_tile;
+
+/*
  * Activation quantization, 1x128 tiles (per token per 128 channels).
  *
  *   x      bf16  [M, K], row stride ldx (elements)            (input)
@@ -117,6 +131,15 @@ fp8bs_status fp8bs_gemm(const uint8_t *qa, const float *sa, const uint8_t *qw, c
                         int64_t ldc, fp8bs_stream_t stream);
 
 /*
+ * fp8bs_gemm with an explicit output tile (FP8BS_ERR_INVALID_ARG for an
+ * unknown tile or PAIR_256x256 with N % 256 != 0).
+ */
+fp8bs_status fp8bs_gemm_tiled(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                              const float *sw, void *c, fp8bs_out_dtype out_dtype, int64_t M,
+                              int64_t N, int64_t K, int64_t ldc, fp8bs_tile tile,
+                              fp8bs_stream_t stream);
+
+/*
  * Grouped (MoE) GEMM: for each expert e, rows r in
  * [expert_offsets[e], expert_offsets[e+1]) of A are multiplied by W_e:
  * C[r, :] = A_hat[r, :] * W_hat_e^T.
@@ -138,6 +161,13 @@ fp8bs_status fp8bs_grouped_gemm(const uint8_t *qa, const float *sa, const int32_
                                 int32_t E, int64_t total_M, const uint8_t *qw, const float *sw,
                                 void *c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
                                 int64_t ldc, fp8bs_stream_t stream);
+
+/* fp8bs_grouped_gemm with an explicit output tile (see fp8bs_gemm_tiled). */
+fp8bs_status fp8bs_grouped_gemm_tiled(const uint8_t *qa, const float *sa,
+                                      const int32_t *expert_offsets, int32_t E, int64_t total_M,
+                                      const uint8_t *qw, const float *sw, void *c,
+                                      fp8bs_out_dtype out_dtype, int64_t N, int64_t K, int64_t ldc,
+                                      fp8bs_tile tile, fp8bs_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char *fp8bs_status_string(fp8bs_status status);

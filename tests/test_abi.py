@@ -7,7 +7,8 @@ import pytest
 from fp8_fine_grained_17_b300 import fp8bs
 
 EXPECTED = {"fp8bs_quantize_act_1x128", "fp8bs_quantize_weight_128x128", "fp8bs_gemm",
-            "fp8bs_grouped_gemm", "fp8bs_status_string", "fp8bs_last_device_error"}
+            "fp8bs_grouped_gemm", "fp8bs_gemm_tiled", "fp8bs_grouped_gemm_tiled",
+            "fp8bs_status_string", "fp8bs_last_device_error"}
 
 
 def test_header_declares_the_boundary():
@@ -67,3 +68,14 @@ def test_grouped_argument_checks():
     assert f(P, P, None, 2, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_INVALID_ARG
     assert f(P, P, P, 2, 0, P, P, P, 0, 128, 128, 128, None) == fp8bs.OK                 # no rows
     assert f(P, P, P + 2, 2, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_INVALID_ARG
+
+
+def test_tile_argument_checks():
+    L = fp8bs.lib()
+    f = L.fp8bs_gemm_tiled
+    assert f(P, P, P, P, P, 0, 4, 128, 128, 128, 9, None) == fp8bs.ERR_INVALID_ARG     # unknown tile
+    assert f(P, P, P, P, P, 0, 4, 384, 128, 384, fp8bs.TILE_PAIR_256x256, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, P, P, P, P, 0, 0, 512, 128, 512, fp8bs.TILE_PAIR_256x256, None) == fp8bs.OK
+    g = L.fp8bs_grouped_gemm_tiled
+    assert g(P, P, P, 2, 10, P, P, P, 0, 128, 128, 128, -1, None) == fp8bs.ERR_INVALID_ARG
+    assert g(P, P, P, 2, 0, P, P, P, 0, 256, 128, 256, fp8bs.TILE_PAIR_256x128, None) == fp8bs.OK

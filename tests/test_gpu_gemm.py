@@ -34,9 +34,12 @@ def test_reference_case_f32(orc):
     _run(orc, d.a_bits, d.w_bits, torch.float32)
 
 
+# N % 256 == 0 runs the CTA-pair kernel (256-row tiles), other N the
+# single-CTA kernel (128-row tiles); M covers partial and single-row tiles.
 @pytest.mark.parametrize("M,N,K", [
     (1, 128, 128), (5, 256, 128), (127, 128, 256), (129, 384, 512),
     (300, 640, 1024), (257, 1152, 384), (128, 256, 4096),
+    (1, 256, 128), (255, 512, 256), (257, 768, 384), (513, 256, 640), (640, 1280, 1152),
 ])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_shapes(orc, M, N, K, out):
@@ -100,3 +103,36 @@ def test_full_workloads(orc, cfg):
     d = getattr(wl, cfg)(0)
     worst = _run(orc, d.a_bits, d.w_bits, torch.bfloat16)
     print(f"{cfg}: worst err/tol = {worst:.3g}")
+
+
+@pytest.mark.parametrize("tile", [fp8bs.TILE_128x256, fp8bs.TILE_128x128,
+                                  fp8bs.TILE_PAIR_256x256, fp8bs.TILE_PAIR_256x128])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (257, 512, 384), (600, 768, 1024)])
+def test_every_tile_shape(orc, tile, M, N, K):
+    """Each output tile (single CTA 128x256 / 128x128, CTA pair 256x256 /
+    256x128) against the oracle, with partial row tiles."""
+    rng = np.random.default_rng(M + N + K + tile)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = gpu_quant_act(a)
+    qw, sw = gpu_quant_weight(w)
+    c = fp8bs.gemm(qa, sa, qw, sw, torch.float32, tile=tile)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
+    check_gemm(c, C_or, B, False)
+
+
+def test_tiles_bit_identical():
+    """Every tile shape accumulates each output in the same order, so all
+    give the same bits (M=1000, N=1536, K=2048, bf16 out)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    M, N, K = 1000, 1536, 2048
+    qa = torch.randint(0, 0x7F, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+    qw = torch.randint(0, 0x7F, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+    sa = torch.rand((M, K // 128), device="cuda", generator=g) * 1e-2
+    sw = torch.rand((N // 128, K // 128), device="cuda", generator=g) * 1e-2
+    outs = [fp8bs.gemm(qa, sa, qw, sw, torch.bfloat16, tile=t) for t in fp8bs.TILES]
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])

@@ -109,3 +109,22 @@ def test_moe_full_workload_sampled(orc):
             assert np.all(err <= tol), (e, nb, np.max(err / tol))
             worst = max(worst, float(np.max(err / tol)))
     print(f"moe sampled worst err/tol {worst:.3g}")
+
+
+@pytest.mark.parametrize("tile", [fp8bs.TILE_128x256, fp8bs.TILE_128x128,
+                                  fp8bs.TILE_PAIR_256x256, fp8bs.TILE_PAIR_256x128])
+def test_grouped_every_tile(orc, tile):
+    """Empty, single-row and multi-tile experts through every tile shape."""
+    counts = [0, 300, 1, 129, 0, 520]
+    d = wl.moe(seed=11, N=512, K=384, counts=counts)
+    qa, sa = gpu_quant_act(d.a_bits)
+    qw, sw = _quant_experts(orc, d.w_bits, check=False)
+    off = torch.from_numpy(d.offsets).cuda()
+    c = fp8bs.grouped_gemm(qa, sa, off, qw, sw, torch.float32, tile=tile)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    E, N, K = d.w_bits.shape
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    q_o, s_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K),
+                               s_o.reshape(E, N // 128, K // 128))
+    check_gemm(c, C_or, B, False)
