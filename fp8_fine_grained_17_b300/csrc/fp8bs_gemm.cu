@@ -33,13 +33,11 @@
 //               next free TMEM slot, overwriting it (the chunk's partial
 //               P_kb).
 //   warp 2      TMEM allocator (512 columns).
-//   warp 3      builds the expert tile table (a dense launch is one expert),
-//               then loads scales: each chunk's 128 activation scales and two
-//               weight-block scales into an 8-slot shared-memory ring with
-//               cp.async, running up to 8 chunks ahead of the promotion.
-//   warps 4-11  promotion: each thread owns one row and kBN/2 columns; per
-//               chunk it reads P_kb from TMEM (tcgen05.ld, the next 16
-//               columns in flight while the current ones are accumulated),
+//   warp 3      builds the expert tile table (a dense launch is one expert).
+//   warps 4-11  promotion: each thread owns one row and kBN/2 columns; its
+//               scales come straight from global memory, four chunks at a
+//               time, one batch ahead of use. Per chunk it reads P_kb from
+//               TMEM (tcgen05.ld, loads in flight during the FMAs),
 //               frees the buffer, and accumulates acc += (sa * sw) * P_kb in
 //               FP32 registers with the packed FMA pipe. After the last chunk
 //               it converts and stores its row segment.
@@ -59,10 +57,10 @@ namespace {
 
 constexpr int BM = 128;   // output rows per CTA (TMEM lanes)
 constexpr int BK = 128;   // K chunk = one scale group
-constexpr int kScaleStages = 8;
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr int kMaxExperts = 1024;
+constexpr int kMaxExperts = 512;
+constexpr int kEpiRowBytes = 80;
 constexpr int kProducerRegs = 56;
 constexpr int kEpilogueRegs = 224;
 
@@ -89,13 +87,13 @@ struct __align__(1024) Smem {
     uint64_t tmem_full[C::kSlots];
     uint64_t tmem_empty[C::kSlots];       // even CTA: 8 arrivals per CTA of the pair
     uint64_t drain;
-    uint64_t scale_full[kScaleStages];    // 32 cp.async arrivals (one per loader lane)
-    uint64_t scale_empty[kScaleStages];   // 8 arrivals (one per promotion warp)
-    float scale_a[kScaleStages][BM];      // sa[row0 + r, kb]
-    float scale_w[kScaleStages][4];       // sw[e, (n0 + h kBN/2)/128, kb], h = 0, 1
     uint32_t tmem_base;
     int abort;
     int num_tiles;
+    // Epilogue staging, one buffer per promotion warp: 32 rows x 64 bytes,
+    // rows 80 bytes apart so that 16-byte writes of a quarter warp hit
+    // distinct banks.
+    alignas(16) uint8_t epi[8][32 * kEpiRowBytes];
     int tile_start[kMaxExperts + 1];   // first tile index of each expert
     int row_start[kMaxExperts + 1];    // copy of expert_offsets
 };
@@ -157,6 +155,32 @@ __device__ __forceinline__ Tile decode_tile(const Smem<kCtas, kBN>& sm, const Pa
     tile.expert = e;
     tile.b_row0 = e * p.N + tile.n0;
     return tile;
+}
+
+// The tiles of one work unit (CTA, or CTA pair): unit, unit + n_units, ...,
+// each as the K-chunk range [k0, k1) = [0, KB).
+struct Segments {
+    int t, step, num_tiles, KB;
+    __device__ __forceinline__ bool next(int& tile, int& k0, int& k1)
+    {
+        if (t >= num_tiles)
+            return false;
+        tile = t;
+        k0 = 0;
+        k1 = KB;
+        t += step;
+        return true;
+    }
+};
+
+__device__ __forceinline__ Segments work_of(const Params& p, int num_tiles, int unit, int n_units)
+{
+    Segments w;
+    w.KB = p.KB;
+    w.num_tiles = num_tiles;
+    w.t = unit;
+    w.step = n_units;
+    return w;
 }
 
 // Warp 3: copy and validate expert_offsets (a dense launch uses {0, M}),
@@ -228,8 +252,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     // per pair.
     const uint32_t rank = kCtas == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const int first_tile = static_cast<int>(blockIdx.x) / kCtas;
-    const int tile_step = static_cast<int>(gridDim.x) / kCtas;
+    const int unit = static_cast<int>(blockIdx.x) / kCtas;      // work unit of this CTA
+    const int n_units = static_cast<int>(gridDim.x) / kCtas;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -241,10 +265,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             mbar_init(smem_addr(&sm.tmem_empty[b]), 8 * kCtas);   // one per promotion warp
         }
         mbar_init(smem_addr(&sm.drain), 1);
-        for (int s = 0; s < kScaleStages; ++s) {
-            mbar_init(smem_addr(&sm.scale_full[s]), 32);
-            mbar_init(smem_addr(&sm.scale_empty[s]), 8);
-        }
         sm.abort = 0;
         fence_barrier_init();
     }
@@ -276,11 +296,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             uint32_t chunk = 0;
             uint32_t s = 0, ph = 0;   // stage and its phase parity
             bool ok = true;
-            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
+            Segments work = work_of(p, num_tiles, unit, n_units);
+            int t, k0, k1;
+            while (ok && work.next(t, k0, k1)) {
                 const Tile tile = decode_tile(sm, p, t);
                 const int32_t a_row = static_cast<int32_t>(tile.m0) + static_cast<int32_t>(rank) * BM;
                 const int32_t b_row = tile.b_row0 + static_cast<int32_t>(rank) * C::kBRows;
-                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
+                for (int kb = k0; kb < k1; ++kb, ++chunk) {
                     const bool ready = mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err);
                     if (!__all_sync(0xFFFFFFFFu, ready)) {
                         ok = false;
@@ -335,8 +357,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // >> 4 to the start-address field (shared addresses < 256 KB).
             const uint64_t adesc0 = smem_desc_k_sw128(smem_addr(sm.a[0]));
             const uint64_t bdesc0 = smem_desc_k_sw128(smem_addr(sm.b[0]));
-            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
-                for (int kb = 0; kb < p.KB; ++kb) {
+            Segments work = work_of(p, num_tiles, unit, n_units);
+            int t, k0, k1;
+            while (ok && work.next(t, k0, k1)) {
+                for (int kb = k0; kb < k1; ++kb) {
                     const uint32_t empty_bar = smem_addr(&sm.tmem_empty[b]);
                     const uint32_t full_bar = smem_addr(&sm.full[s]);
                     // Both conditions are usually met already: test them
@@ -378,40 +402,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 mbar_wait_drain(smem_addr(&sm.drain), 0, kWaitLimitNs, p.err);
             }
             __syncwarp();
-        } else if (warp == 3) {
-            // ---------------------------------------------------- scale loader
-            uint32_t chunk = 0;
-            bool ok = true;
-            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
-                const Tile tile = decode_tile(sm, p, t);
-                // Rows past the tile's end read a valid row; their products
-                // are never stored.
-                const float* src_a[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int64_t row = tile.m0 + rank * BM + lane + 32 * i;
-                    src_a[i] = p.sa + (row < p.rows ? row : p.rows - 1) * p.KB;
-                }
-                const int nbh = min((tile.n0 + (lane & 1) * C::kCols) / 128, p.NB - 1);
-                const float* src_w = p.sw + (static_cast<int64_t>(tile.expert) * p.NB + nbh) * p.KB;
-                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                    const uint32_t s = chunk % kScaleStages;
-                    const uint32_t ph = (chunk / kScaleStages) & 1u;
-                    const bool ready =
-                        mbar_wait(smem_addr(&sm.scale_empty[s]), ph ^ 1u, abort_flag, p.err);
-                    if (!__all_sync(0xFFFFFFFFu, ready)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        cp_async_4(smem_addr(&sm.scale_a[s][lane + 32 * i]), src_a[i] + kb);
-                    if (lane < 2)
-                        cp_async_4(smem_addr(&sm.scale_w[s][lane]), src_w + kb);
-                    cp_async_arrive_noinc(smem_addr(&sm.scale_full[s]));
-                }
-            }
-            cp_async_wait_all();
         }
     } else {
         regs_inc<kEpilogueRegs>();
@@ -425,18 +415,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                                                 : map_to_cta(smem_addr(&sm.tmem_empty[0]), 0);
         uint32_t chunk = 0;
         bool ok = true;
-        // Scale of chunk c: sa[row, kb] * sw[n-block, kb] from the scale ring;
-        // the slot goes back to the loader right after the read.
-        auto take_scale = [&](uint32_t c, float& scale) -> bool {
-            const uint32_t ss = c % kScaleStages;
-            const bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), (c / kScaleStages) & 1u,
-                                         abort_flag, p.err);
-            scale = ready ? sm.scale_a[ss][r] * sm.scale_w[ss][half] : 0.0f;
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_addr(&sm.scale_empty[ss]));
-            return ready;
-        };
         auto give_slot = [&](uint32_t c) {
             tc_fence_before();
             __syncwarp();
@@ -447,181 +425,170 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     mbar_arrive_remote(tmem_empty0 + 8 * (c % C::kSlots));
             }
         };
-        if constexpr (C::kCols == 64) {
-            // Each chunk: both 32-column loads in flight at once, one wait,
-            // the slot goes back, then the arithmetic.
-            // acquire: scale and TMEM load (issued, not waited) of chunk c.
-            auto acquire = [&](uint32_t c, uint32_t (&x0)[32], uint32_t (&x1)[32], float& scale) -> bool {
-                bool ready = take_scale(c, scale);
-                const uint32_t b = c % C::kSlots;
-                ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), (c / C::kSlots) & 1u,
-                                           abort_flag, p.err);
-                if (!__all_sync(0xFFFFFFFFu, ready))
-                    return false;
-                tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * C::kCols;
+        // Promotes chunk c with the given scale into acc; false if the wait
+        // gave up.
+        auto promote = [&](uint32_t c, float scale, float2 (&acc)[C::kCols / 2]) -> bool {
+            const uint32_t b = c % C::kSlots;
+            const bool ready = mbar_wait(smem_addr(&sm.tmem_full[b]), (c / C::kSlots) & 1u,
+                                         abort_flag, p.err);
+            // The warp continues only if every lane saw the phases complete:
+            // the TMEM loads below are warp-collective.
+            if (!__all_sync(0xFFFFFFFFu, ready))
+                return false;
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * C::kCols;
+            const float2 scale2 = make_float2(scale, scale);
+            if constexpr (C::kCols == 64) {
+                // Both 32-column loads in flight at once, one wait, the slot
+                // goes back, then the arithmetic.
+                uint32_t x0[32], x1[32];
                 tmem_ld_32x32b_x32(taddr, x0);
                 tmem_ld_32x32b_x32(taddr + 32, x1);
-                return true;
-            };
-            auto complete = [&](uint32_t c, uint32_t (&x0)[32], uint32_t (&x1)[32]) {
                 tmem_ld_wait(x0);
                 tmem_ld_tie(x1);
                 give_slot(c);
-            };
-            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
-                const Tile tile = decode_tile(sm, p, t);
-                const int64_t row = tile.m0 + rank * BM + r;
-                const int n_col = tile.n0 + half * C::kCols;
-                const bool live = row < tile.row_end && n_col < p.N;
-                float2 acc[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    acc[i] = make_float2(0.0f, 0.0f);
-                auto accumulate = [&](uint32_t (&x0)[32], uint32_t (&x1)[32], float scale) {
-                    const float2 scale2 = make_float2(scale, scale);
+                for (int i = 0; i < 16; ++i)
+                    acc[i] = __ffma2_rn(
+                        make_float2(__uint_as_float(x0[2 * i]), __uint_as_float(x0[2 * i + 1])),
+                        scale2, acc[i]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[i] = __ffma2_rn(
-                            make_float2(__uint_as_float(x0[2 * i]), __uint_as_float(x0[2 * i + 1])),
-                            scale2, acc[i]);
+                for (int i = 0; i < 16; ++i)
+                    acc[16 + i] = __ffma2_rn(
+                        make_float2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1])),
+                        scale2, acc[16 + i]);
+            } else {
+                // Column blocks j of 16: the load of block j+1 is in flight
+                // while block j is accumulated; the slot goes back once the
+                // last load has completed.
+                constexpr int kBlocks = C::kCols / 16;
+                uint32_t v[2][16];
+                tmem_ld_32x32b_x16(taddr, v[0]);
+                tmem_ld_wait(v[0]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[16 + i] = __ffma2_rn(
-                            make_float2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1])),
-                            scale2, acc[16 + i]);
-                };
-#pragma unroll 1
-                for (int kb = 0; kb < p.KB; ++kb) {
-                    uint32_t x0[32], x1[32];
-                    float scale;
-                    if (!acquire(chunk + kb, x0, x1, scale)) {
-                        ok = false;
-                        break;
-                    }
-                    complete(chunk + kb, x0, x1);
-                    accumulate(x0, x1, scale);
-                }
-                chunk += p.KB;
-                if (!ok)
-                    break;
-                if (ok && live) {
-                    if (p.out_bf16) {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + row * p.ldc + n_col;
+                for (int j = 0; j < kBlocks; ++j) {
+                    if (j + 1 < kBlocks)
+                        tmem_ld_32x32b_x16(taddr + 16 * (j + 1), v[(j + 1) & 1]);
+                    else
+                        give_slot(c);
 #pragma unroll
-                        for (int i = 0; i < C::kCols / 8; ++i) {
-                            uint4 pk;
-                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
-                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
-                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
-                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
-                            memcpy(&pk.x, &h0, 4);
-                            memcpy(&pk.y, &h1, 4);
-                            memcpy(&pk.z, &h2, 4);
-                            memcpy(&pk.w, &h3, 4);
-                            reinterpret_cast<uint4*>(dst)[i] = pk;
-                        }
-                    } else {
-                        float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
-#pragma unroll
-                        for (int i = 0; i < C::kCols / 4; ++i)
-                            reinterpret_cast<float4*>(dst)[i] = make_float4(
-                                acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        acc[8 * j + i] = __ffma2_rn(make_float2(__uint_as_float(v[j & 1][2 * i]),
+                                                                __uint_as_float(v[j & 1][2 * i + 1])),
+                                                    scale2, acc[8 * j + i]);
+                    if (j + 1 < kBlocks)
+                        tmem_ld_wait(v[(j + 1) & 1]);
                 }
             }
-        } else {
-            uint32_t chunk = 0;
-            bool ok = true;
-            for (int t = first_tile; t < num_tiles && ok; t += tile_step) {
-                const Tile tile = decode_tile(sm, p, t);
-                const int64_t row = tile.m0 + rank * BM + r;
-                const int n_col = tile.n0 + half * C::kCols;
-                const bool live = row < tile.row_end && n_col < p.N;
+            return true;
+        };
+        Segments work = work_of(p, num_tiles, unit, n_units);
+        int t, k0, k1;
+        while (ok && work.next(t, k0, k1)) {
+            const Tile tile = decode_tile(sm, p, t);
+            const int n_col = tile.n0 + half * C::kCols;
 
-                // kCols FP32 accumulators as pairs for the packed FMA pipe.
-                float2 acc[C::kCols / 2];
+            // kCols FP32 accumulators as pairs for the packed FMA pipe.
+            float2 acc[C::kCols / 2];
 #pragma unroll
-                for (int i = 0; i < C::kCols / 2; ++i)
-                    acc[i] = make_float2(0.0f, 0.0f);
-    #pragma unroll 1
-                for (int kb = 0; kb < p.KB; ++kb, ++chunk) {
-                    const uint32_t ss = chunk % kScaleStages;
-                    const uint32_t sph = (chunk / kScaleStages) & 1u;
-                    const uint32_t b = chunk % C::kSlots;
-                    const uint32_t tph = (chunk / C::kSlots) & 1u;
-                    // The warp continues only if every lane saw the phases
-                    // complete: the TMEM loads below are warp-collective.
-                    bool ready = mbar_wait(smem_addr(&sm.scale_full[ss]), sph, abort_flag, p.err);
-                    float scale = 0.0f;
-                    if (ready)
-                        scale = sm.scale_a[ss][r] * sm.scale_w[ss][half];
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_addr(&sm.scale_empty[ss]));
-                    ready = ready && mbar_wait(smem_addr(&sm.tmem_full[b]), tph, abort_flag, p.err);
-                    if (!__all_sync(0xFFFFFFFFu, ready)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t taddr =
-                        tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * C::kCols;
-                    const float2 scale2 = make_float2(scale, scale);
-                    // Column blocks j of 16: the load of block j+1 is in flight
-                    // while block j is accumulated.
-                    constexpr int kBlocks = C::kCols / 16;
-                    uint32_t v[2][16];
-                    tmem_ld_32x32b_x16(taddr, v[0]);
-                    tmem_ld_wait(v[0]);
-#pragma unroll
-                    for (int j = 0; j < kBlocks; ++j) {
-                        if (j + 1 < kBlocks)
-                            tmem_ld_32x32b_x16(taddr + 16 * (j + 1), v[(j + 1) & 1]);
-                        else {
-                            // Every TMEM read of this buffer has been issued and
-                            // waited for: hand it back.
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) {
-                                if (kCtas == 1)
-                                    mbar_arrive(tmem_empty0 + 8 * b);
-                                else
-                                    mbar_arrive_remote(tmem_empty0 + 8 * b);
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            acc[8 * j + i] = __ffma2_rn(make_float2(__uint_as_float(v[j & 1][2 * i]),
-                                                                    __uint_as_float(v[j & 1][2 * i + 1])),
-                                                        scale2, acc[8 * j + i]);
-                        if (j + 1 < kBlocks)
-                            tmem_ld_wait(v[(j + 1) & 1]);
-                    }
+            for (int i = 0; i < C::kCols / 2; ++i)
+                acc[i] = make_float2(0.0f, 0.0f);
+            // Scales straight from global memory: a thread's activation
+            // scales sa[row, :] are contiguous, and the warp's weight scales
+            // sw[e, n-block, :] are one broadcast address. They are read four
+            // chunks at a time, one batch ahead of use (latency hidden), and
+            // rotated as chunks are consumed. Rows past the end read the last
+            // row; their results are never stored.
+            const int64_t srow = min(tile.m0 + rank * BM + r, p.rows - 1);
+            const float* sa_row = p.sa + srow * p.KB;
+            const float* sw_row =
+                p.sw + (static_cast<int64_t>(tile.expert) * p.NB + min(n_col / 128, p.NB - 1)) * p.KB;
+            auto load4 = [&](int kb0, float4& a4, float4& w4) {
+                const int last = p.KB - 1;
+                a4 = make_float4(__ldg(sa_row + min(kb0, last)), __ldg(sa_row + min(kb0 + 1, last)),
+                                 __ldg(sa_row + min(kb0 + 2, last)), __ldg(sa_row + min(kb0 + 3, last)));
+                w4 = make_float4(__ldg(sw_row + min(kb0, last)), __ldg(sw_row + min(kb0 + 1, last)),
+                                 __ldg(sw_row + min(kb0 + 2, last)), __ldg(sw_row + min(kb0 + 3, last)));
+            };
+            float4 cs;       // sa * sw of the current batch, rotated per chunk
+            float4 na, nw;   // next batch, in flight
+            if (k1 > k0) {
+                load4(k0, na, nw);
+                cs = make_float4(na.x * nw.x, na.y * nw.y, na.z * nw.z, na.w * nw.w);
+                load4(k0 + 4, na, nw);
+            }
+#pragma unroll 1
+            for (int kb = k0; kb < k1; ++kb, ++chunk) {
+                if (kb > k0 && ((kb - k0) & 3) == 0) {
+                    cs = make_float4(na.x * nw.x, na.y * nw.y, na.z * nw.z, na.w * nw.w);
+                    load4(kb + 4, na, nw);
                 }
-                if (ok && live) {
-                    if (p.out_bf16) {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + row * p.ldc + n_col;
+                if (!promote(chunk, cs.x, acc)) {
+                    ok = false;
+                    break;
+                }
+                cs = make_float4(cs.y, cs.z, cs.w, 0.0f);
+            }
+            if (!ok)
+                break;
+
+            // Epilogue through the warp's staging buffer: each thread writes
+            // 64 bytes of its own row, then every store instruction writes 8
+            // rows x 64 contiguous bytes of C. Rows past the tile's end (M
+            // tail, or the next expert's rows) are not written.
+            if (n_col < p.N) {
+                uint8_t* buf = sm.epi[warp - 4];
+                const int64_t row0 = tile.m0 + rank * BM + quarter * 32;   // row of lane 0
+                const int rl = lane >> 2;    // read phase: rows rl + 8 i, 16-byte chunk lane & 3
+                const int ch = lane & 3;
+                if (p.out_bf16) {
 #pragma unroll
-                        for (int i = 0; i < C::kCols / 8; ++i) {
+                    for (int j = 0; j < C::kCols / 32; ++j) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
                             uint4 pk;
-                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[4 * i + 0]);
-                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[4 * i + 1]);
-                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[4 * i + 2]);
-                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[4 * i + 3]);
+                            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[16 * j + 4 * k + 0]);
+                            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[16 * j + 4 * k + 1]);
+                            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[16 * j + 4 * k + 2]);
+                            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[16 * j + 4 * k + 3]);
                             memcpy(&pk.x, &h0, 4);
                             memcpy(&pk.y, &h1, 4);
                             memcpy(&pk.z, &h2, 4);
                             memcpy(&pk.w, &h3, 4);
-                            reinterpret_cast<uint4*>(dst)[i] = pk;
+                            *reinterpret_cast<uint4*>(buf + lane * kEpiRowBytes + 16 * k) = pk;
                         }
-                    } else {
-                        float* dst = static_cast<float*>(p.c) + row * p.ldc + n_col;
+                        __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < C::kCols / 4; ++i)
-                            reinterpret_cast<float4*>(dst)[i] = make_float4(
-                                acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = rl + 8 * i;
+                            const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * kEpiRowBytes + 16 * ch);
+                            const int64_t grow = row0 + rr;
+                            if (grow < tile.row_end)
+                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.c) + grow * p.ldc +
+                                                          n_col + 32 * j + 8 * ch) = v;
+                        }
+                        __syncwarp();
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::kCols / 16; ++j) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<float4*>(buf + lane * kEpiRowBytes + 16 * k) =
+                                make_float4(acc[8 * j + 2 * k].x, acc[8 * j + 2 * k].y,
+                                            acc[8 * j + 2 * k + 1].x, acc[8 * j + 2 * k + 1].y);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = rl + 8 * i;
+                            const float4 v = *reinterpret_cast<const float4*>(buf + rr * kEpiRowBytes + 16 * ch);
+                            const int64_t grow = row0 + rr;
+                            if (grow < tile.row_end)
+                                *reinterpret_cast<float4*>(static_cast<float*>(p.c) + grow * p.ldc + n_col +
+                                                           16 * j + 4 * ch) = v;
+                        }
+                        __syncwarp();
                     }
                 }
             }
@@ -720,8 +687,9 @@ fp8bs_status configure_once(int device, int sm_count, int* max_units)
 }
 
 // rows: rows of A; w_rows: rows of the stacked W. The number of tiles is
-// computed on the device from the expert table; the grid is the resident
-// maximum, capped by an upper bound of the tiles.
+// computed on the device from the expert table (a dense launch is one
+// expert); the grid is the resident maximum, capped by an upper bound of the
+// tiles.
 template <int kCtas, int kBN>
 fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
                     int64_t K, cudaStream_t stream)
@@ -734,7 +702,7 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     p.err = device_error_word();
     if (p.err == nullptr)
         return FP8BS_ERR_CUDA;
-    p.n_tiles = p.N / kBN;
+    p.n_tiles = (p.N + kBN - 1) / kBN;   // a last partial tile is masked
     const int64_t tile_bound = (rows / C::kTileRows + p.E) * static_cast<int64_t>(p.n_tiles);
     if (tile_bound > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
@@ -750,10 +718,10 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     st = configure_once<kCtas, kBN>(info.device, info.sm_count, &max_units);
     if (st != FP8BS_OK)
         return st;
+    const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
     const int units = static_cast<int>(tile_bound < max_units ? tile_bound : max_units);
     if (units <= 0)
         return FP8BS_OK;
-    const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
     if (kCtas == 1) {
         kernel<<<units, kThreads, smem_bytes<kCtas, kBN>(), stream>>>(map_a, map_b, p);
         return launch_status();

@@ -155,7 +155,7 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *qa, const float *sa, const uint8_t 
  *   c                [total_M, N], row stride ldc; rows not covered by any
  *                    expert are left untouched
  *
- * 1 <= E <= 1024; K % 128 == 0, N % 128 == 0. Same accuracy as fp8bs_gemm.
+ * 1 <= E <= 512; K % 128 == 0, N % 128 == 0. Same accuracy as fp8bs_gemm.
  */
 fp8bs_status fp8bs_grouped_gemm(const uint8_t *qa, const float *sa, const int32_t *expert_offsets,
                                 int32_t E, int64_t total_M, const uint8_t *qw, const float *sw,

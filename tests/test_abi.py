@@ -64,7 +64,7 @@ def test_gemm_argument_checks():
 def test_grouped_argument_checks():
     f = fp8bs.lib().fp8bs_grouped_gemm
     assert f(P, P, P, 0, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_INVALID_ARG   # E = 0
-    assert f(P, P, P, 1025, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_UNSUPPORTED
+    assert f(P, P, P, 513, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_UNSUPPORTED
     assert f(P, P, None, 2, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_INVALID_ARG
     assert f(P, P, P, 2, 0, P, P, P, 0, 128, 128, 128, None) == fp8bs.OK                 # no rows
     assert f(P, P, P + 2, 2, 10, P, P, P, 0, 128, 128, 128, None) == fp8bs.ERR_INVALID_ARG

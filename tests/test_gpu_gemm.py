@@ -107,10 +107,13 @@ def test_full_workloads(orc, cfg):
 
 @pytest.mark.parametrize("tile", [fp8bs.TILE_128x256, fp8bs.TILE_128x128,
                                   fp8bs.TILE_PAIR_256x256, fp8bs.TILE_PAIR_256x128])
-@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (257, 512, 384), (600, 768, 1024)])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (257, 512, 384), (600, 768, 1024),
+                                   (300, 384, 512)])
 def test_every_tile_shape(orc, tile, M, N, K):
     """Each output tile (single CTA 128x256 / 128x128, CTA pair 256x256 /
     256x128) against the oracle, with partial row tiles."""
+    if tile == fp8bs.TILE_PAIR_256x256 and N % 256:
+        pytest.skip("the pair's 256-wide tile needs N % 256 == 0 (rejected, see test_abi)")
     rng = np.random.default_rng(M + N + K + tile)
     a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
     w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
@@ -123,11 +126,11 @@ def test_every_tile_shape(orc, tile, M, N, K):
 
 
 def test_tiles_bit_identical():
-    """Every tile shape accumulates each output in the same order, so all
-    give the same bits (M=1000, N=1536, K=2048, bf16 out)."""
+    """Every tile shape accumulates each output in the same order (chunk by
+    chunk, one FMA per chunk), so all give the same bits."""
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
-    M, N, K = 1000, 1536, 2048
+    M, N, K = 4736, 1024, 1024
     qa = torch.randint(0, 0x7F, (M, K), dtype=torch.uint8, device="cuda", generator=g)
     qw = torch.randint(0, 0x7F, (N, K), dtype=torch.uint8, device="cuda", generator=g)
     sa = torch.rand((M, K // 128), device="cuda", generator=g) * 1e-2
@@ -136,3 +139,4 @@ def test_tiles_bit_identical():
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
