@@ -167,6 +167,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Contiguous bulk copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from global to this CTA's shared memory; completion counted in
+// bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // 2-D tiled load of box (x, y) into shared memory; completion is counted in
 // bytes on `bar`. x is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -23,6 +23,7 @@
 // fma, bf16x2 magnitude max), and the per-group scalar work (amax/448 and its
 // reciprocal) is done once per group, spread over the lanes that share it.
 #include <cstdint>
+#include <mutex>
 
 #include "fp8bs_device.cuh"
 #include "fp8bs_host.h"
@@ -110,24 +111,59 @@ __device__ __forceinline__ uint2 quantize8(const uint4& v, const Divider& d)
 // ---------------------------------------------------------------------------
 // Activation quantizer.
 //
-// Four consecutive lanes (a quad) own four consecutive 1x128 groups per
-// iteration; lane t of the quad loads the 16-byte chunks t, t+4, t+8, t+12 of
-// each group, so one warp-wide load instruction touches 8 groups x 64
-// contiguous bytes. The quad's four partial maxima are reduced with a
-// transposing exchange (3 shuffles) that leaves group t's amax in lane t;
-// lane t computes that group's scale and reciprocal and writes the scale
-// (the warp writes 32 consecutive scales), and the quad broadcasts them. All
-// loads of an iteration (256 B per lane) are issued before any arithmetic.
-// kContiguous: rows are back to back (ld == K), so group g starts at element
-// 128 g and no row/column split is needed.
+// Work unit: a lane quad (four consecutive lanes) and four 1x128 groups.
+// Lane t of the quad holds the 16-byte chunks t + 4 ((j + rot) & 3),
+// j = 0..3, of each of the four groups (rot lets two quads that share a
+// shared-memory bank group start at different chunks). The quad's four
+// partial maxima are reduced with a transposing exchange (3 shuffles) that
+// leaves group t's amax in lane t; lane t computes that group's scale and
+// reciprocal once and writes the scale, and the quad broadcasts them.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void quantize_quad(const uint4 (&v)[4][4], const bool (&valid)[4],
+                                              uint8_t* const (&qdst)[4], float* my_scale, int t,
+                                              int quad_base, int rot)
+{
+    uint32_t m[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        m[u] = absmax_words(v[u], 4);
+    // Transposing max-exchange: after it lane t holds group t's amax.
+    const bool b1 = (t & 2) != 0, b0 = (t & 1) != 0;
+    uint32_t k[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b1 ? m[i] : m[2 + i], 2);
+        k[i] = max(b1 ? m[2 + i] : m[i], recv);
+    }
+    const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b0 ? k[0] : k[1], 1);
+    const uint32_t mine = max(b0 ? k[1] : k[0], recv);
+
+    const Divider own = make_divider(bf16_bits_to_f32(mine));
+    if (my_scale != nullptr)
+        *my_scale = own.s;
+
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        Divider d;
+        d.s = __shfl_sync(0xFFFFFFFFu, own.s, quad_base + u);
+        d.r = __shfl_sync(0xFFFFFFFFu, own.r, quad_base + u);
+        if (valid[u]) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                __stcs(reinterpret_cast<uint2*>(qdst[u] + 8 * (t + 4 * ((j + rot) & 3))),
+                       quantize8(v[u][j], d));
+        }
+    }
+}
+
+// Strided rows: a grid-stride loop over 32-group blocks per warp; all loads
+// of an iteration (256 B per lane) are issued before any arithmetic.
 constexpr int kActThreads = 256;
 
-template <bool kContiguous>
 __global__ void __launch_bounds__(kActThreads)
-quantize_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
-                    int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
-                    int64_t total_groups)
+quantize_act_strided_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
+                            int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
+                            int64_t total_groups)
 {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
@@ -137,57 +173,126 @@ quantize_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __rest
 
     for (int64_t base = warp * 32; base < total_groups; base += n_warps * 32) {
         uint4 v[4][4];
-        int64_t xoff[4], qoff[4];
+        uint8_t* qdst[4];
         bool valid[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t g = base + quad_base + u;
             valid[u] = g < total_groups;
-            if (kContiguous) {
-                xoff[u] = g * 128;
-                qoff[u] = g * 128;
-            } else {
-                const int64_t row = valid[u] ? g / groups_per_row : 0;
-                const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
-                xoff[u] = row * ldx + col;
-                qoff[u] = row * ldq + col;
-            }
-            const uint4* src = reinterpret_cast<const uint4*>(x + (valid[u] ? xoff[u] : 0)) + t;
+            const int64_t row = valid[u] ? g / groups_per_row : 0;
+            const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
+            qdst[u] = q + row * ldq + col;
+            const uint4* src = reinterpret_cast<const uint4*>(x + row * ldx + col) + t;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
         }
+        const int64_t my_g = base + lane;   // scale is [M, K/128] row-major: index = g
+        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, 0);
+    }
+}
 
-        uint32_t m[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            m[u] = absmax_words(v[u], 4);
-        // Transposing max-exchange: after it lane t holds group t's amax.
-        const bool b1 = (t & 2) != 0, b0 = (t & 1) != 0;
-        uint32_t k[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b1 ? m[i] : m[2 + i], 2);
-            k[i] = max(b1 ? m[2 + i] : m[i], recv);
+// Contiguous rows (ld == K): the input is one stream of 256-byte groups. A
+// CTA of 4 warps takes 128-group chunks (32 KB) in a grid-stride order and
+// keeps a 3-stage ring of them in flight with bulk asynchronous copies
+// (cp.async.bulk, mbarrier-tracked), so the loads of the next two chunks are
+// outstanding while one is quantized from shared memory.
+constexpr int kTmaThreads = 128;
+constexpr int kTmaChunkGroups = 128;
+constexpr int kTmaChunkBytes = kTmaChunkGroups * 256;
+constexpr int kTmaStages = 3;
+
+struct __align__(128) ActSmem {
+    uint8_t stage[kTmaStages][kTmaChunkBytes];
+    uint64_t full[kTmaStages];
+    int abort;
+};
+constexpr size_t kActSmemBytes = sizeof(ActSmem) + 128;
+
+__global__ void __launch_bounds__(kTmaThreads)
+quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ q,
+                           float* __restrict__ scale, int64_t total_groups, unsigned int* err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    ActSmem& sm = *reinterpret_cast<ActSmem*>(smem_raw + (((raw + 127u) & ~127u) - raw));
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t = lane & 3;
+    const int quad_base = lane & ~3;
+    const int rot = (lane >> 2) & 1;
+    const int64_t n_chunks = (total_groups + kTmaChunkGroups - 1) / kTmaChunkGroups;
+
+    auto issue = [&](int64_t c, int s) {
+        const int64_t g0 = c * kTmaChunkGroups;
+        const int64_t n = min(static_cast<int64_t>(kTmaChunkGroups), total_groups - g0);
+        const uint32_t bar = smem_addr(&sm.full[s]);
+        const uint32_t bytes = static_cast<uint32_t>(n * 256);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(smem_addr(sm.stage[s]), x + g0 * 128, bytes, bar);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTmaStages; ++s)
+            mbar_init(smem_addr(&sm.full[s]), 1);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (c < n_chunks)
+                issue(c, s);
         }
-        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b0 ? k[0] : k[1], 1);
-        const uint32_t mine = max(b0 ? k[1] : k[0], recv);
-
-        const Divider own = make_divider(bf16_bits_to_f32(mine));
-        if (base + lane < total_groups)
-            scale[base + lane] = own.s;   // scale is [M, K/128] row-major: index = g
-
+    }
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const bool ready = mbar_wait(smem_addr(&sm.full[s]), ph, &sm.abort, err);
+        if (!__syncthreads_and(ready)) {
+            // A wait gave up (reported in err): let the copies still in
+            // flight land (bounded waits) before the CTA leaves.
+            if (threadIdx.x == 0) {
+                int ds = s;
+                uint32_t dph = ph;
+                for (int i = 0; i < kTmaStages; ++i) {
+                    if (c + static_cast<int64_t>(i) * gridDim.x < n_chunks)
+                        mbar_wait_drain(smem_addr(&sm.full[ds]), dph, kWaitLimitNs, err);
+                    if (++ds == kTmaStages) {
+                        ds = 0;
+                        dph ^= 1u;
+                    }
+                }
+            }
+            break;
+        }
+        const int64_t g0 = c * kTmaChunkGroups;
+        const int lq = warp * 32 + quad_base;   // first of the quad's four groups in the chunk
+        uint4 v[4][4];
+        uint8_t* qdst[4];
+        bool valid[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            Divider d;
-            d.s = __shfl_sync(0xFFFFFFFFu, own.s, quad_base + u);
-            d.r = __shfl_sync(0xFFFFFFFFu, own.r, quad_base + u);
-            if (valid[u]) {
-                uint8_t* dst = q + qoff[u] + t * 8;
+            const int64_t g = g0 + lq + u;
+            valid[u] = g < total_groups;
+            qdst[u] = q + g * 128;
+            const uint8_t* src = sm.stage[s] + (lq + u) * 256;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    __stcs(reinterpret_cast<uint2*>(dst + 32 * j), quantize8(v[u][j], d));
-            }
+            for (int j = 0; j < 4; ++j)
+                v[u][j] = valid[u] ? *reinterpret_cast<const uint4*>(src + 16 * (t + 4 * ((j + rot) & 3)))
+                                   : make_uint4(0, 0, 0, 0);
+        }
+        const int64_t my_g = g0 + warp * 32 + lane;
+        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, rot);
+        __syncthreads();   // every thread is done with stage s
+        if (threadIdx.x == 0) {
+            const int64_t c2 = c + static_cast<int64_t>(kTmaStages) * gridDim.x;
+            if (c2 < n_chunks)
+                issue(c2, s);
+        }
+        if (++s == kTmaStages) {
+            s = 0;
+            ph ^= 1u;
         }
     }
 }
@@ -245,24 +350,20 @@ quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
     }
 }
 
-template <bool kContiguous>
-int act_grid(const DeviceInfo& info, int64_t total_groups)
+// Resident CTAs of a kernel on the device (cached per kernel; at least 1).
+template <typename Kernel>
+int resident_blocks(Kernel kernel, int threads, size_t smem, int* cache)
 {
-    static int blocks_per_sm = 0;
-    if (blocks_per_sm == 0) {
+    if (*cache == 0) {
         int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_act_kernel<kContiguous>,
-                                                          kActThreads, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess ||
             b <= 0) {
             cudaGetLastError();
-            b = 2;
+            b = 1;
         }
-        blocks_per_sm = b;
+        *cache = b;
     }
-    const int64_t groups_per_block = (kActThreads / 32) * 32;
-    const int64_t needed = (total_groups + groups_per_block - 1) / groups_per_block;
-    const int64_t full = static_cast<int64_t>(info.sm_count) * blocks_per_sm;
-    return static_cast<int>(needed < full ? needed : full);
+    return *cache;
 }
 
 }  // namespace
@@ -296,11 +397,39 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (ldx == K && ldq == K) {
-        quantize_act_kernel<true><<<act_grid<true>(info, total), kActThreads, 0, s>>>(
-            xb, ldx, q, ldq, scale, G, total);
+        static std::mutex mu;
+        static bool configured[64] = {};
+        static int per_sm = 0;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (info.device < 0 || info.device >= 64)
+                return FP8BS_ERR_CUDA;
+            if (!configured[info.device]) {
+                if (cudaFuncSetAttribute(quantize_act_contig_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kActSmemBytes)) != cudaSuccess) {
+                    cudaGetLastError();
+                    return FP8BS_ERR_CUDA;
+                }
+                configured[info.device] = true;
+            }
+            resident_blocks(quantize_act_contig_kernel, kTmaThreads, kActSmemBytes, &per_sm);
+        }
+        unsigned int* err = device_error_word();
+        if (err == nullptr)
+            return FP8BS_ERR_CUDA;
+        const int64_t chunks = (total + kTmaChunkGroups - 1) / kTmaChunkGroups;
+        const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
+        const int grid = static_cast<int>(chunks < full ? chunks : full);
+        quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err);
     } else {
-        quantize_act_kernel<false><<<act_grid<false>(info, total), kActThreads, 0, s>>>(
-            xb, ldx, q, ldq, scale, G, total);
+        static int per_sm = 0;
+        resident_blocks(quantize_act_strided_kernel, kActThreads, 0, &per_sm);
+        const int64_t per_block = (kActThreads / 32) * 32;
+        const int64_t needed = (total + per_block - 1) / per_block;
+        const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
+        const int grid = static_cast<int>(needed < full ? needed : full);
+        quantize_act_strided_kernel<<<grid, kActThreads, 0, s>>>(xb, ldx, q, ldq, scale, G, total);
     }
     return launch_status();
 }
