@@ -156,14 +156,16 @@ __device__ __forceinline__ void quantize_quad(const uint4 (&v)[4][4], const bool
     }
 }
 
-// Strided rows: a grid-stride loop over 32-group blocks per warp; all loads
+// Register path: a grid-stride loop over 32-group blocks per warp; all loads
 // of an iteration (256 B per lane) are issued before any arithmetic.
+// kContiguous: rows back to back (ld == K), group g starts at element 128 g.
 constexpr int kActThreads = 256;
 
+template <bool kContiguous>
 __global__ void __launch_bounds__(kActThreads)
-quantize_act_strided_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
-                            int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
-                            int64_t total_groups)
+quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
+                         int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
+                         int64_t total_groups)
 {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
@@ -179,10 +181,18 @@ quantize_act_strided_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t
         for (int u = 0; u < 4; ++u) {
             const int64_t g = base + quad_base + u;
             valid[u] = g < total_groups;
-            const int64_t row = valid[u] ? g / groups_per_row : 0;
-            const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
-            qdst[u] = q + row * ldq + col;
-            const uint4* src = reinterpret_cast<const uint4*>(x + row * ldx + col) + t;
+            int64_t xo, qo;
+            if (kContiguous) {
+                xo = valid[u] ? g * 128 : 0;
+                qo = xo;
+            } else {
+                const int64_t row = valid[u] ? g / groups_per_row : 0;
+                const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
+                xo = row * ldx + col;
+                qo = row * ldq + col;
+            }
+            qdst[u] = q + qo;
+            const uint4* src = reinterpret_cast<const uint4*>(x + xo) + t;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
@@ -192,15 +202,20 @@ quantize_act_strided_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t
     }
 }
 
-// Contiguous rows (ld == K): the input is one stream of 256-byte groups. A
-// CTA of 4 warps takes 128-group chunks (32 KB) in a grid-stride order and
-// keeps a 3-stage ring of them in flight with bulk asynchronous copies
-// (cp.async.bulk, mbarrier-tracked), so the loads of the next two chunks are
-// outstanding while one is quantized from shared memory.
+// Large contiguous inputs (ld == K, at least kTmaMinGroups groups): the
+// input is one stream of 256-byte groups. A CTA of 4 warps takes 128-group
+// chunks (32 KB) in a grid-stride order and keeps a 3-stage ring of them in
+// flight with bulk asynchronous copies (cp.async.bulk, mbarrier-tracked), so
+// the loads of the next two chunks are outstanding while one is quantized
+// from shared memory. For smaller inputs each CTA gets only a few chunks and
+// the ring's fill latency dominates; the register path is faster there
+// (measured on B300: [4096, 7168] 22.9 us register path vs 25.2 us ring;
+// [16384, 7168] 68.9 us vs 67.7 us).
 constexpr int kTmaThreads = 128;
 constexpr int kTmaChunkGroups = 128;
 constexpr int kTmaChunkBytes = kTmaChunkGroups * 256;
 constexpr int kTmaStages = 3;
+constexpr int64_t kTmaMinGroups = int64_t(1) << 19;
 
 struct __align__(128) ActSmem {
     uint8_t stage[kTmaStages][kTmaChunkBytes];
@@ -396,7 +411,7 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
     const int64_t total = M * G;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    if (ldx == K && ldq == K) {
+    if (ldx == K && ldq == K && total >= kTmaMinGroups) {
         static std::mutex mu;
         static bool configured[64] = {};
         static int per_sm = 0;
@@ -423,13 +438,21 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
         const int grid = static_cast<int>(chunks < full ? chunks : full);
         quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err);
     } else {
-        static int per_sm = 0;
-        resident_blocks(quantize_act_strided_kernel, kActThreads, 0, &per_sm);
+        const bool contiguous = ldx == K && ldq == K;
+        static int per_sm[2] = {0, 0};
         const int64_t per_block = (kActThreads / 32) * 32;
         const int64_t needed = (total + per_block - 1) / per_block;
-        const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
-        const int grid = static_cast<int>(needed < full ? needed : full);
-        quantize_act_strided_kernel<<<grid, kActThreads, 0, s>>>(xb, ldx, q, ldq, scale, G, total);
+        if (contiguous) {
+            resident_blocks(quantize_act_regs_kernel<true>, kActThreads, 0, &per_sm[1]);
+            const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[1];
+            quantize_act_regs_kernel<true><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
+                                             s>>>(xb, ldx, q, ldq, scale, G, total);
+        } else {
+            resident_blocks(quantize_act_regs_kernel<false>, kActThreads, 0, &per_sm[0]);
+            const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[0];
+            quantize_act_regs_kernel<false><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
+                                              s>>>(xb, ldx, q, ldq, scale, G, total);
+        }
     }
     return launch_status();
 }

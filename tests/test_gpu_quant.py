@@ -86,22 +86,36 @@ def _pair_rows(a_lo: int, a_hi: int) -> np.ndarray:
     return rows
 
 
+# The activation quantizer streams large contiguous inputs through a shared-
+# memory ring of bulk copies and takes smaller ones through registers; both
+# paths are checked on every pair.
+RING_MIN_GROUPS = 1 << 19
+
+
 @pytest.mark.slow
 def test_exhaustive_amax_x_pairs(orc):
     """All ~1.07e9 (amax, x) pairs: the code of one element depends only on its
     group's amax and its own value, so this covers the quantizer's whole
-    input space, including subnormal scales and the small-amax path."""
+    input space, including subnormal scales and the small-amax path. Each
+    slice runs through both kernel paths: alone (register path) and padded
+    with all-zero groups to the ring path's minimum size."""
     edges = np.linspace(1, 0x7F80, 49).astype(np.int64)
     pool = ThreadPoolExecutor(max_workers=8)
     total = 0
     for lo, hi in zip(edges[:-1], edges[1:]):
         rows = _pair_rows(int(lo), int(hi))
         total += rows.size
+        assert rows.shape[0] < RING_MIN_GROUPS
         q, s = gpu_quant_act(rows)
+        padded = np.zeros((RING_MIN_GROUPS, 128), dtype=np.uint16)
+        padded[:rows.shape[0]] = rows
+        qp, sp = gpu_quant_act(padded)
         parts = np.array_split(np.arange(rows.shape[0]), 8)
         res = list(pool.map(lambda ix: orc.quantize_act_1x128(rows[ix]), parts))
         q_or = np.concatenate([r[0] for r in res])
         s_or = np.concatenate([r[1] for r in res])
         check_codes(q, s, q_or, s_or)
+        check_codes(qp[:rows.shape[0]], sp[:rows.shape[0]], q_or, s_or)
+        assert torch.all(qp[rows.shape[0]:] == 0) and torch.all(sp[rows.shape[0]:] == 1.0)
     pool.shutdown()
     assert total > 1.07e9
