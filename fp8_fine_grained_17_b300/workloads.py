@@ -165,3 +165,30 @@ def moe(seed: int = 0, N: int = 4096, K: int = 7168, counts=None, with_a: bool =
     a = activations(ra, int(offsets[-1]), K)[0] if with_a else None
     return MoE(f"moe grouped {E} experts N={N} K={K} rows={int(offsets[-1])}",
                counts, offsets, N, K, a, w)
+
+
+def norm_params(rng: np.random.Generator, K: int, with_beta: bool):
+    """Normalization weights as bf16 patterns: gamma ~ 1 + N(0, 0.1^2) [K] and,
+    if asked, beta ~ N(0, 0.02^2) [K]."""
+    gamma = bf16_bits(np.float32(1.0) + rng.standard_normal(K, dtype=np.float32) * np.float32(0.1))
+    beta = bf16_bits(rng.standard_normal(K, dtype=np.float32) * np.float32(0.02)) if with_beta else None
+    return gamma, beta
+
+
+@dataclass
+class Norm:
+    name: str
+    M: int
+    K: int
+    x_bits: np.ndarray
+    gamma_bits: np.ndarray
+    beta_bits: np.ndarray | None
+
+
+def norm(M: int, K: int, seed: int = 0, outlier_scale=100.0, with_beta: bool = False) -> Norm:
+    """Hidden states entering a normalization layer: the activation recipe
+    (N(0,1), 0.5% outlier channels) and the weights of ``norm_params``."""
+    rx, rp = _children(seed + 1000, 2)
+    x, _ = activations(rx, M, K, outlier_scale)
+    gamma, beta = norm_params(rp, K, with_beta)
+    return Norm(f"norm+quant [{M},{K}]", M, K, x, gamma, beta)

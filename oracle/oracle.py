@@ -26,6 +26,11 @@ What it computes, and the passage each step follows:
   post, paragraph on quantizing before the MoE up-projection for FP8 Fprop).
 * Acceptance bound: |C_gpu - C_or| <= 2e-5 * sum_k |A_hat W_hat| + 1e-6, plus
   2^-8 |C_or| for a bf16 output (statement of the problem).
+* Normalization fused with the 1x128 cast (RMSNorm or LayerNorm, bf16
+  output, then the activation quantizer): "How I Improved My Deepseek In In
+  The Future", paragraph of hardware suggestions (fusion of layer
+  normalization and FP8 cast). Row statistics in float64 rounded once to
+  binary32; the elementwise part as binary32 numpy operations.
 """
 from __future__ import annotations
 
@@ -229,3 +234,87 @@ def tolerance(C_or: np.ndarray, B: np.ndarray, out_bf16: bool) -> np.ndarray:
     if out_bf16:
         tol = tol + np.abs(C_or) * 2.0 ** -8
     return tol
+
+
+# ---------------------------------------------------------------------------
+# Normalization fused with the 1x128 cast.
+#
+# "How I Improved My Deepseek In In The Future", paragraph of hardware
+# suggestions: a warp-level cast instruction would allow the layer
+# normalization and the FP8 cast to be fused. Reading taken here: the fused
+# producer computes exactly what a normalization layer with a bf16 output
+# followed by the 1x128 activation quantizer computes. Two kinds:
+#   RMSNorm   y = x * rstd * gamma (+ beta),   rstd = 1/sqrt(mean(x^2) + eps)
+#   LayerNorm y = (x - mu) * rstd * gamma (+ beta),
+#             mu = mean(x), rstd = 1/sqrt(mean((x - mu)^2) + eps)
+# Row statistics are exact in float64 and then rounded once to binary32 (the
+# precision the layer stores them in). The elementwise part is written as
+# binary32 operations in the order above (subtract, multiply by rstd,
+# multiply by gamma, add beta), each rounded to nearest, and the result is
+# rounded to bf16 (nearest-even) before the 1x128 quantizer sees it.
+# ---------------------------------------------------------------------------
+NORM_RMS = 0
+NORM_LAYER = 1
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> the same values as float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(y: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit pattern, rounded to nearest, ties to even.
+
+    The 16 low bits are dropped after adding half an ulp of the result,
+    less one when the kept part is even (so that an exact half goes to the
+    even neighbour). Finite inputs only."""
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep_odd = (u >> 16) & 1
+    return ((u + 0x7FFF + keep_odd) >> 16).astype(np.uint16)
+
+
+def norm_stats(x_bits: np.ndarray, kind: int, eps: float):
+    """Row statistics (mu, rstd) as float32 [M]; mu is 0 for RMSNorm."""
+    x = bf16_bits_to_f32(x_bits).astype(np.float64)
+    eps64 = float(np.float32(eps))
+    M, K = x.shape
+    if kind == NORM_RMS:
+        mu = np.zeros(M)
+        var = (x * x).sum(axis=1) / K
+    elif kind == NORM_LAYER:
+        mu = x.sum(axis=1) / K
+        d = x - mu[:, None]
+        var = (d * d).sum(axis=1) / K
+    else:
+        raise ValueError(f"unknown normalization kind {kind}")
+    rstd = 1.0 / np.sqrt(var + eps64)
+    return mu.astype(np.float32), rstd.astype(np.float32)
+
+
+def norm_apply(x_bits, gamma_bits, beta_bits, kind: int, mu32, rstd32) -> np.ndarray:
+    """bf16 patterns of the normalized rows, given binary32 row statistics."""
+    x = bf16_bits_to_f32(x_bits)
+    mu32 = np.asarray(mu32, dtype=np.float32)[:, None]
+    rstd32 = np.asarray(rstd32, dtype=np.float32)[:, None]
+    d = x - mu32 if kind == NORM_LAYER else x
+    t = d * rstd32
+    u = t * bf16_bits_to_f32(gamma_bits)[None, :]
+    y = u + bf16_bits_to_f32(beta_bits)[None, :] if beta_bits is not None else u
+    return f32_to_bf16_bits(y)
+
+
+def norm_quantize_act_1x128(x_bits, gamma_bits, beta_bits, kind: int, eps: float,
+                            mu32=None, rstd32=None):
+    """Normalize each row, round to bf16, quantize in 1x128 tiles.
+
+    Returns (q uint8 [M, K], s float32 [M, K/128], mu float32 [M],
+    rstd float32 [M], y uint16 [M, K]). Given mu32/rstd32 (for example a
+    kernel's own statistics, already checked against norm_stats), the
+    elementwise part and the quantizer use those, so that every rounding
+    that decides a code is taken from the same binary32 statistics."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    if mu32 is None or rstd32 is None:
+        mu32, rstd32 = norm_stats(x_bits, kind, eps)
+    y = norm_apply(x_bits, gamma_bits, beta_bits, kind, mu32, rstd32)
+    q, s = quantize_act_1x128(y)
+    return q, s, np.asarray(mu32, np.float32), np.asarray(rstd32, np.float32), y
