@@ -9,13 +9,14 @@ output. The headline value is GEMM FLOPs over the whole step's time
 
 * the activation quantizer alone on [16384, 7168] with 0.5% outlier channels
   (GB/s against the HBM roofline),
+* RMSNorm fused with the 1x128 cast on the same [16384, 7168] shape,
 * the GEMM M=4096, N=7168, K=2048 with 0.5% outlier channels x50,
 * the MoE grouped GEMM (32 experts, N=4096, K=7168, seeded top-8 routing),
 * the end-to-end step from pinned host buffers (`e2e`),
 * the CPU oracle on a bounded sample (`cpu_baseline`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--part all|step|act_quant|gemm2|moe] [--skip-cpu]
+                  [--part all|step|act_quant|norm_quant|gemm2|moe] [--skip-cpu]
 
 With --gpus N > 1 (launched by torchrun) every rank runs the same step on its
 own GPU with no collective on the data path (independent replicas, weak
@@ -292,6 +293,48 @@ def bench_act_quant(fp8bs, dev, stream, peaks, args):
             "timing": f"median of {n} launches"}
 
 
+def bench_norm_quant(fp8bs, dev, stream, peaks, args):
+    """RMSNorm fused with the 1x128 cast on [16384, 7168] (0.5% outlier
+    channels x100), alternating between two seeded inputs (470 MB > L2)."""
+    ns = [wl.norm(16384, 7168, seed=s) for s in (0, 1)]
+    xs = [wl.bits_to_torch(n.x_bits).to(dev) for n in ns]
+    g = wl.bits_to_torch(ns[0].gamma_bits).to(dev)
+    M, K = xs[0].shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+
+    def call(i):
+        fp8bs.fp8bs_norm_quantize_act_1x128(xs[i % 2], g, None, fp8bs.NORM_RMS, 1e-6, q, s,
+                                            None, rstd, stream)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            call(i)
+    n = max(20, min(args.steps, 200))
+    evs = _events(n)
+    with torch.cuda.stream(stream):
+        for i, (e0, e1) in enumerate(evs):
+            e0.record(stream)
+            call(i)
+            e1.record(stream)
+    stream.synchronize()
+    ms = _median_ms(evs)
+    groups = M * (K // 128)
+    nbytes = groups * (256 + 128 + 4) + M * 4 + K * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "RMSNorm + act-quant [16384,7168] bf16, 36 outlier channels x100",
+            "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "bytes": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "norm_quant_kernel",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": _traffic("norm_quant_kernel", "norm-quant 16384x7168"),
+                         "algorithmic": f"{groups} groups x 388 B (256 B read, 128 B codes, "
+                                        f"4 B scale) + 4 B rstd per row + gamma",
+                         "peak_note": f"of {peaks['source']} copy bandwidth"},
+            "l2": "two 235 MB inputs alternated (> 126 MB L2)",
+            "timing": f"median of {n} launches"}
+
+
 def bench_gemm2(fp8bs, dev, stream, peaks, args):
     """GEMM M=4096, N=7168, K=2048 (0.5% outlier channels x50), pre-quantized
     operands, bf16 out; operands of 3 seeded sets rotated."""
@@ -431,7 +474,8 @@ def run_ours(args, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
-    parts = {"all": ("step", "act_quant", "gemm2", "moe", "e2e")}.get(args.part, (args.part,))
+    parts = {"all": ("step", "act_quant", "norm_quant", "gemm2", "moe", "e2e")}.get(
+        args.part, (args.part,))
 
     result = {}
     if "step" in parts:
@@ -455,6 +499,9 @@ def run_ours(args, world):
         torch.cuda.empty_cache()
     if "act_quant" in parts:
         result["act_quant"] = bench_act_quant(fp8bs, dev, stream, peaks, args)
+        torch.cuda.empty_cache()
+    if "norm_quant" in parts:
+        result["norm_quant"] = bench_norm_quant(fp8bs, dev, stream, peaks, args)
         torch.cuda.empty_cache()
     if "gemm2" in parts:
         result["gemm_4096x7168x2048"] = bench_gemm2(fp8bs, dev, stream, peaks, args)
@@ -557,7 +604,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--part", choices=["all", "step", "act_quant", "gemm2", "moe", "e2e"],
+    ap.add_argument("--part", choices=["all", "step", "act_quant", "norm_quant", "gemm2", "moe", "e2e"],
                     default="all", help="which measurements to run (profiling uses one)")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle CPU baseline")
     args = ap.parse_args()

@@ -12,8 +12,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfp8bs.so")
-SOURCES = ["fp8bs_common.cu", "fp8bs_quant.cu", "fp8bs_gemm.cu"]
-HEADERS = ["fp8bs_device.cuh", "fp8bs_host.h"]
+SOURCES = ["fp8bs_common.cu", "fp8bs_quant.cu", "fp8bs_norm.cu", "fp8bs_gemm.cu"]
+HEADERS = ["fp8bs_device.cuh", "fp8bs_e4m3.cuh", "fp8bs_host.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 # No fast-math: the quantizers must round every binary32 operation as IEEE does.

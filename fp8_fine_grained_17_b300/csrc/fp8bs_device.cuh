@@ -468,6 +468,14 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
     return d;
 }
 
+// a + b per half.
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // a * b + c per half, fused (one rounding).
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
 {
@@ -509,6 +517,16 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
 {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two binary32 values (lo, hi halves of a packed pair) to two bf16 values in
+// one word, each rounded to nearest even; lo lands in the low 16 bits.
+__device__ __forceinline__ uint32_t cvt_bf16x2(uint64_t v)
+{
+    const float2 f = unpack_f32x2(v);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
     return r;
 }
 

@@ -22,6 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 OUT_F32, OUT_BF16 = 0, 1
 TILE_AUTO, TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128 = 0, 1, 2, 3, 4
 TILES = (TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128)
+NORM_RMS, NORM_LAYER = 0, 1
 
 
 class Fp8bsError(RuntimeError):
@@ -58,6 +59,9 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_grouped_gemm_tiled.argtypes = [vp, f32p, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
                                                i64, i64, i64, ctypes.c_int, vp]
         L.fp8bs_grouped_gemm_tiled.restype = st
+        L.fp8bs_norm_quantize_act_1x128.argtypes = [vp, i64, i64, i64, vp, vp, ctypes.c_int,
+                                                    ctypes.c_float, vp, i64, f32p, f32p, f32p, vp]
+        L.fp8bs_norm_quantize_act_1x128.restype = st
         L.fp8bs_status_string.argtypes = [ctypes.c_int]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
@@ -126,6 +130,24 @@ def fp8bs_quantize_weight_128x128(w: torch.Tensor, q: torch.Tensor, scale: torch
         _ptr(w), N, K, _row_stride(w), _ptr(q8), _row_stride(q8), _ptr(scale), _stream(stream)))
 
 
+def fp8bs_norm_quantize_act_1x128(x: torch.Tensor, gamma: torch.Tensor, beta, kind: int, eps: float,
+                                  q: torch.Tensor, scale: torch.Tensor, mean=None, rstd=None,
+                                  stream=None):
+    """RMSNorm/LayerNorm of x bf16 [M, K] (gamma, optional beta: bf16 [K]),
+    rounded to bf16 and cast in 1x128 tiles: q [M, K], scale fp32 [M, K/128];
+    optional fp32 [M] outputs mean (LayerNorm) and rstd."""
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16 and gamma.dtype == torch.bfloat16 and gamma.is_contiguous()
+    assert beta is None or (beta.dtype == torch.bfloat16 and beta.is_contiguous())
+    assert scale.dtype == torch.float32 and scale.is_contiguous()
+    for t in (mean, rstd):
+        assert t is None or (t.dtype == torch.float32 and t.is_contiguous())
+    q8 = _u8(q)
+    _check("fp8bs_norm_quantize_act_1x128", lib().fp8bs_norm_quantize_act_1x128(
+        _ptr(x), M, K, _row_stride(x), _ptr(gamma), _ptr(beta), int(kind), float(eps),
+        _ptr(q8), _row_stride(q8), _ptr(scale), _ptr(mean), _ptr(rstd), _stream(stream)))
+
+
 def _out_dtype(c: torch.Tensor) -> int:
     if c.dtype == torch.float32:
         return OUT_F32
@@ -178,6 +200,18 @@ def quantize_act(x: torch.Tensor, stream=None):
     s = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
     fp8bs_quantize_act_1x128(x, q, s, stream)
     return q, s
+
+
+def norm_quantize_act(x: torch.Tensor, gamma: torch.Tensor, beta=None, kind: int = NORM_RMS,
+                      eps: float = 1e-6, stream=None):
+    """Returns (q, scale, mean, rstd); mean is None for RMSNorm."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
+    mean = torch.empty(M, dtype=torch.float32, device=x.device) if kind == NORM_LAYER else None
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    fp8bs_norm_quantize_act_1x128(x, gamma, beta, kind, eps, q, s, mean, rstd, stream)
+    return q, s, mean, rstd
 
 
 def quantize_weight(w: torch.Tensor, stream=None):

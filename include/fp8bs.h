@@ -95,6 +95,44 @@ fp8bs_status fp8bs_quantize_act_1x128(const void *x, int64_t M, int64_t K, int64
                                       uint8_t *q, int64_t ldq, float *scale,
                                       fp8bs_stream_t stream);
 
+/* Normalization applied by fp8bs_norm_quantize_act_1x128. */
+typedef enum { FP8BS_NORM_RMS = 0, FP8BS_NORM_LAYER = 1 } fp8bs_norm_kind;
+
+/*
+ * Normalization fused with the 1x128 activation cast -- "How I Improved My
+ * Deepseek In In The Future", paragraph of hardware suggestions (fusion of
+ * layer normalization and FP8 cast). Produces exactly what a normalization
+ * layer with a bf16 output followed by fp8bs_quantize_act_1x128 produces,
+ * without writing the normalized tensor to memory.
+ *
+ *   x      bf16  [M, K], row stride ldx (elements)            (input)
+ *   gamma  bf16  [K]                                          (input)
+ *   beta   bf16  [K] or NULL (no additive term)               (input)
+ *   q      e4m3  [M, K], row stride ldq (bytes)               (output codes)
+ *   scale  fp32  [M, K/128] row-major, contiguous             (output)
+ *   mean   fp32  [M] or NULL; written for LayerNorm only      (output)
+ *   rstd   fp32  [M] or NULL                                  (output)
+ *
+ * Per row, in binary32 with each step rounded to nearest:
+ *   RMSNorm   (FP8BS_NORM_RMS):   mu = 0,       v = sum_k x^2 / K
+ *   LayerNorm (FP8BS_NORM_LAYER): mu = sum_k x / K, v = sum_k (x - mu)^2 / K
+ *   rstd = 1 / sqrt(v + eps)   (correctly rounded)
+ *   y = bf16_rne(((x - mu) * rstd) * gamma + beta)
+ * and then the 1x128 quantizer on y (codes and scales as in
+ * fp8bs_quantize_act_1x128). The two sums are formed in a parallel order, so
+ * mu and rstd may differ from a sequentially summed value by a few units in
+ * the last place; given the returned mu and rstd, q and scale are exact.
+ * K % 128 == 0 and 0 < K <= 65536 (else FP8BS_ERR_UNSUPPORTED; K == 0 with
+ * M > 0 is FP8BS_ERR_INVALID_ARG); eps finite and >= 0 (eps == 0 with a
+ * row whose v is 0 gives rstd = inf and non-finite y, outside the contract).
+ * gamma and beta must be 16-byte aligned.
+ */
+fp8bs_status fp8bs_norm_quantize_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                           const void *gamma, const void *beta,
+                                           fp8bs_norm_kind kind, float eps, uint8_t *q,
+                                           int64_t ldq, float *scale, float *mean, float *rstd,
+                                           fp8bs_stream_t stream);
+
 /*
  * Weight quantization, 128x128 blocks (per 128 input x 128 output channels).
  *

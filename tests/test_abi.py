@@ -8,7 +8,7 @@ from fp8_fine_grained_17_b300 import fp8bs
 
 EXPECTED = {"fp8bs_quantize_act_1x128", "fp8bs_quantize_weight_128x128", "fp8bs_gemm",
             "fp8bs_grouped_gemm", "fp8bs_gemm_tiled", "fp8bs_grouped_gemm_tiled",
-            "fp8bs_status_string", "fp8bs_last_device_error"}
+            "fp8bs_norm_quantize_act_1x128", "fp8bs_status_string", "fp8bs_last_device_error"}
 
 
 def test_header_declares_the_boundary():
@@ -79,3 +79,22 @@ def test_tile_argument_checks():
     g = L.fp8bs_grouped_gemm_tiled
     assert g(P, P, P, 2, 10, P, P, P, 0, 128, 128, 128, -1, None) == fp8bs.ERR_INVALID_ARG
     assert g(P, P, P, 2, 0, P, P, P, 0, 256, 128, 256, fp8bs.TILE_PAIR_256x128, None) == fp8bs.OK
+
+
+def test_norm_argument_checks():
+    f = fp8bs.lib().fp8bs_norm_quantize_act_1x128
+    R, L_ = fp8bs.NORM_RMS, fp8bs.NORM_LAYER
+    assert f(P, 0, 128, 128, P, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.OK      # M = 0
+    assert f(P, -1, 128, 128, P, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 100, 128, P, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_UNSUPPORTED
+    assert f(P, 4, 65536 + 128, 65536 + 128, P, None, R, 1e-6, P, 65536 + 128, P, None, None,
+             None) == fp8bs.ERR_UNSUPPORTED                                                 # K too large
+    assert f(P, 4, 0, 0, P, None, R, 1e-6, P, 0, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # K = 0
+    assert f(P, 4, 128, 128, P, None, 2, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # kind
+    assert f(P, 4, 128, 128, P, None, L_, -1.0, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # eps
+    assert f(P, 4, 128, 128, P, None, L_, float("nan"), P, 128, P, None, None,
+             None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 128, 128, None, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # gamma
+    assert f(P, 4, 128, 128, P, P + 8, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # beta align
+    assert f(P, 4, 128, 128, P, None, R, 1e-6, P, 128, P, P + 2, None, None) == fp8bs.ERR_INVALID_ARG  # mean align
+    assert f(P, 4, 128, 120, P, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # ldx < K

@@ -1,0 +1,129 @@
+"""RMSNorm / LayerNorm fused with the 1x128 cast on the GPU against the oracle.
+
+The row statistics come from parallel sums, so they are checked against the
+oracle's float64 statistics within the bound of that summation; the codes and
+scales are then compared bit for bit with the oracle run on the kernel's own
+binary32 statistics (every rounding that decides a code taken from the same
+numbers on both sides)."""
+import numpy as np
+import pytest
+import torch
+
+from fp8_fine_grained_17_b300 import fp8bs
+from fp8_fine_grained_17_b300 import workloads as wl
+from oracle import oracle as orc
+
+from helpers import check_codes, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+U32 = 2.0 ** -24
+
+
+def _stat_bound(K):
+    # Each binary32 square (or centred square) enters a chain of at most
+    # K/64 + 1 lane-local additions, 5 butterfly levels and up to 8 warp
+    # partials: relative error of the sum <= (K/64 + 15) u. 1/sqrt halves it;
+    # the division, +eps and the rounded 1/sqrt add 3 u, and the oracle's
+    # own rounding to binary32 one more.
+    return ((K / 64 + 15) / 2 + 4) * U32
+
+
+def run_norm(x_bits, g_bits, b_bits, kind, eps, ldx=None, ldq=None):
+    M, K = x_bits.shape
+    ldx = ldx or K
+    ldq = ldq or K
+    xs = torch.zeros((M, ldx), dtype=torch.bfloat16, device="cuda")
+    xs[:, :K] = to_dev_bf16(x_bits)
+    x = xs[:, :K]
+    g = to_dev_bf16(g_bits)
+    b = to_dev_bf16(b_bits) if b_bits is not None else None
+    qs = torch.full((M, ldq), 0xA5, dtype=torch.uint8, device="cuda")
+    q = qs[:, :K]
+    s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    mean = torch.full((M,), -7.0, dtype=torch.float32, device="cuda")
+    rstd = torch.empty(M, dtype=torch.float32, device="cuda")
+    fp8bs.fp8bs_norm_quantize_act_1x128(x, g, b, kind, eps, q, s, mean, rstd)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    if ldq > K:   # padding bytes untouched
+        assert torch.all(qs[:, K:] == 0xA5).item()
+    return q, s, mean.cpu().numpy(), rstd.cpu().numpy()
+
+
+def check_norm(x_bits, g_bits, b_bits, kind, eps, q, s, mean_k, rstd_k, rows=None):
+    """Compare the listed rows (all by default)."""
+    q = q.cpu().numpy() if torch.is_tensor(q) else q
+    s = s.cpu().numpy() if torch.is_tensor(s) else s
+    if rows is not None:
+        x_bits = x_bits[rows]
+        q, s = q[rows], s[rows]
+        mean_k, rstd_k = mean_k[rows], rstd_k[rows]
+    K = x_bits.shape[1]
+    mu_or, r_or = orc.norm_stats(x_bits, kind, eps)
+    rel = np.abs(rstd_k.astype(np.float64) - r_or) / r_or
+    assert rel.max() <= _stat_bound(K), f"rstd off by {rel.max() / U32:.1f} u"
+    if kind == orc.NORM_LAYER:
+        mag = np.abs(orc.bf16_bits_to_f32(x_bits).astype(np.float64)).mean(axis=1)
+        err = np.abs(mean_k.astype(np.float64) - mu_or)
+        assert np.all(err <= (K / 64 + 16) * U32 * mag + U32 * np.abs(mu_or))
+        mu = mean_k
+    else:
+        mu = np.zeros_like(rstd_k)
+    q_or, s_or, _, _, _ = orc.norm_quantize_act_1x128(x_bits, g_bits, b_bits, kind, eps,
+                                                      mu32=mu, rstd32=rstd_k)
+    check_codes(torch.from_numpy(np.ascontiguousarray(q)), torch.from_numpy(np.ascontiguousarray(s)),
+                q_or, s_or)
+
+
+SHAPES = [(1, 128), (5, 384), (37, 1024), (64, 2048), (33, 4096), (19, 5120), (70, 7168),
+          (9, 8192), (6, 12288), (3, 16384), (2, 24576), (2, 40960), (1, 65536)]
+
+
+@pytest.mark.parametrize("kind", [orc.NORM_RMS, orc.NORM_LAYER])
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_norm_quant_shapes(kind, M, K):
+    n = wl.norm(M, K, seed=M * 7 + K + kind, with_beta=(K // 128) % 2 == 1)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6)
+    check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd)
+
+
+@pytest.mark.parametrize("kind", [orc.NORM_RMS, orc.NORM_LAYER])
+def test_norm_quant_strided(kind):
+    n = wl.norm(45, 1152, seed=3, with_beta=True)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-5, ldx=1160, ldq=1168)
+    check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-5, q, s, mean, rstd)
+
+
+def test_norm_quant_degenerate_rows():
+    # All-zero rows (RMSNorm, eps > 0: y = 0, every code 0, scale 1) and
+    # constant rows (LayerNorm: y = beta), mixed with ordinary rows.
+    n = wl.norm(12, 768, seed=5, with_beta=True)
+    x = n.x_bits.copy()
+    x[[0, 4, 11]] = 0
+    x[[2, 7]] = wl.bf16_bits(np.full(768, -3.25, np.float32))
+    for kind in (orc.NORM_RMS, orc.NORM_LAYER):
+        q, s, mean, rstd = run_norm(x, n.gamma_bits, n.beta_bits, kind, 1e-6)
+        check_norm(x, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd)
+    q, s, _, _ = run_norm(x, n.gamma_bits, None, orc.NORM_RMS, 1e-6)
+    assert torch.all(q[[0, 4, 11]] == 0).item() and torch.all(s[[0, 4, 11]] == 1.0).item()
+
+
+def test_norm_quant_matches_unfused_gpu_quantizer():
+    # The fused kernel's codes equal the 1x128 quantizer kernel applied to the
+    # normalized bf16 rows (here formed on the host from the kernel's own
+    # statistics), so the fusion changes nothing but the memory traffic.
+    n = wl.norm(96, 7168, seed=8, with_beta=False)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, None, orc.NORM_RMS, 1e-6)
+    y = orc.norm_apply(n.x_bits, n.gamma_bits, None, orc.NORM_RMS, np.zeros_like(rstd), rstd)
+    q2, s2 = fp8bs.quantize_act(to_dev_bf16(y))
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+
+
+@pytest.mark.parametrize("kind", [orc.NORM_RMS, orc.NORM_LAYER])
+def test_norm_quant_full_size_sampled(kind):
+    # [16384, 7168] as benchmarked (0.5% outlier channels x100); rows are
+    # independent, so a seeded sample of 256 rows is compared exactly.
+    n = wl.norm(16384, 7168, seed=0, with_beta=kind == orc.NORM_LAYER)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6)
+    rows = np.sort(np.random.default_rng(1).choice(16384, 256, replace=False))
+    rows = np.concatenate([[0, 1, 16382, 16383], rows])
+    check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd, rows=rows)
