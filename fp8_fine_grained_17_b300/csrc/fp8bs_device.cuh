@@ -509,6 +509,31 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b)
     return d;
 }
 
+// Mixed-precision forms (sm_100+): a bf16 operand is widened exactly to
+// binary32 inside the FP32 pipe's add / fma, so no integer unpacking is
+// needed. lo/hi are the halves of a packed bf16 pair.
+
+// (lo + c, hi + c) as a binary32 pair; with c = -0 this is the exact widening
+// (x + -0 = x for every x, including -0).
+__device__ __forceinline__ uint64_t bf16x2_add_f32(uint32_t w, float c)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(c));
+    return pack_f32x2(lo, hi);
+}
+
+// acc0 += lo * lo, acc1 += hi * hi (fused, binary32 accumulators).
+__device__ __forceinline__ void bf16x2_sq_acc(uint32_t w, float& acc0, float& acc1)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %1, h, h, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w));
+}
+
 // --------------------------------------------------------------- conversions
 
 // Two binary32 values to two E4M3 codes (round to nearest even, saturating to

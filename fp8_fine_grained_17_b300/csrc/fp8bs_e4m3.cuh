@@ -83,6 +83,30 @@ __device__ __forceinline__ uint32_t quantize2_exact(uint32_t w, float s)
                       __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), s));
 }
 
+// quantize2_fast with the bf16 pair widened on the FP32 pipe (same result).
+__device__ __forceinline__ uint32_t quantize2_fast_fp(uint32_t w, uint64_t ns2, uint64_t r2)
+{
+    const uint64_t x = bf16x2_add_f32(w, -0.0f);
+    const uint64_t y0 = mul_f32x2(x, r2);
+    const uint64_t e = fma_f32x2(y0, ns2, x);     // x - y0 * s
+    const float2 y = unpack_f32x2(fma_f32x2(e, r2, y0));
+    return cvt_e4m3x2(y.x, y.y);
+}
+
+// 8 bf16 (one uint4) -> 8 E4M3 codes (one uint2), fast quotient only (the
+// caller has checked d.r != 0), widening on the FP32 pipe.
+__device__ __forceinline__ uint2 quantize8_fast_fp(const uint4& v, const Divider& d)
+{
+    const uint64_t ns2 = pack_f32x2(-d.s, -d.s);
+    const uint64_t r2 = pack_f32x2(d.r, d.r);
+    const uint32_t c0 = quantize2_fast_fp(v.x, ns2, r2);
+    const uint32_t c1 = quantize2_fast_fp(v.y, ns2, r2);
+    const uint32_t c2 = quantize2_fast_fp(v.z, ns2, r2);
+    const uint32_t c3 = quantize2_fast_fp(v.w, ns2, r2);
+    return make_uint2(__byte_perm(c0, c1, 0x5410) | sign_bytes(v.x, v.y),
+                      __byte_perm(c2, c3, 0x5410) | sign_bytes(v.z, v.w));
+}
+
 // 8 bf16 (one uint4) -> 8 E4M3 codes (one uint2), fast quotient only (the
 // caller has checked d.r != 0).
 __device__ __forceinline__ uint2 quantize8_fast(const uint4& v, const Divider& d)
