@@ -10,13 +10,14 @@ output. The headline value is GEMM FLOPs over the whole step's time
 * the activation quantizer alone on [16384, 7168] with 0.5% outlier channels
   (GB/s against the HBM roofline),
 * RMSNorm fused with the 1x128 cast on the same [16384, 7168] shape,
+* the headline step with the activation quantization inside the GEMM kernel,
 * the GEMM M=4096, N=7168, K=2048 with 0.5% outlier channels x50,
 * the MoE grouped GEMM (32 experts, N=4096, K=7168, seeded top-8 routing),
 * the end-to-end step from pinned host buffers (`e2e`),
 * the CPU oracle on a bounded sample (`cpu_baseline`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--part all|step|act_quant|norm_quant|gemm2|moe] [--skip-cpu]
+                  [--part all|step|act_quant|norm_quant|fused|gemm2|moe] [--skip-cpu]
 
 With --gpus N > 1 (launched by torchrun) every rank runs the same step on its
 own GPU with no collective on the data path (independent replicas, weak
@@ -257,6 +258,63 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
     }
 
 
+def bench_fused(fp8bs, dev, stream, peaks, args):
+    """The headline workload with the activation quantization inside the GEMM
+    kernel: quantize W + fused GEMM(bf16 A) per step, on the same rotated
+    input sets; beside it the unfused pair (quantize A, GEMM) on the same
+    inputs, timed the same way."""
+    step_in_bytes = 2 * (M3 * K3 + N3 * K3)
+    n_sets = max(2, -(-3 * L2_BYTES // step_in_bytes))
+    sets = _dense_inputs(n_sets, dev, wl.cfg3)
+    qa = torch.empty((M3, K3), dtype=torch.uint8, device=dev)
+    sa = torch.empty((M3, K3 // 128), dtype=torch.float32, device=dev)
+    qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N3 // 128, K3 // 128), dtype=torch.float32, device=dev)
+    c = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+    n = max(20, min(args.steps, 400))
+
+    def run(fused):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup) + n):
+                a, w = sets[i % n_sets]
+                ev = evs[i - max(3, args.warmup)] if i >= max(3, args.warmup) else None
+                if ev is not None:
+                    ev[0].record(stream)
+                fp8bs.fp8bs_quantize_weight_128x128(w, qw, sw, stream)
+                if ev is not None:
+                    ev[1].record(stream)
+                if fused:
+                    fp8bs.fp8bs_gemm_bf16_act(a, qw, sw, c, stream)
+                else:
+                    fp8bs.fp8bs_quantize_act_1x128(a, qa, sa, stream)
+                    fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+                if ev is not None:
+                    ev[2].record(stream)
+        stream.synchronize()
+        per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs])
+        return per.mean(axis=0)
+
+    flops = 2.0 * M3 * N3 * K3
+    res = {}
+    for rnd in range(2):   # interleaved, two rounds each
+        for fused in (True, False):
+            res.setdefault(fused, []).append(run(fused))
+    assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
+    f_qw, f_g = np.mean(res[True], axis=0)
+    u_qw, u_g = np.mean(res[False], axis=0)
+    del sets
+    return {"workload": "GEMM M=4096,N=4096,K=7168 bf16 A, activation 1x128 quantization "
+                        "inside the GEMM kernel; step = quantize W + fused GEMM",
+            "step_TFLOP/s": round(flops / ((f_qw + f_g) * 1e-3) / 1e12, 1),
+            "fused_gemm_us": round(f_g * 1e3, 2),
+            "fused_gemm_TFLOP/s": round(flops / (f_g * 1e-3) / 1e12, 1),
+            "unfused_step_TFLOP/s": round(flops / ((u_qw + u_g) * 1e-3) / 1e12, 1),
+            "unfused_quantA_plus_gemm_us": round(u_g * 1e3, 2),
+            "timing": f"mean of {n} steps x 2 interleaved rounds per variant, "
+                      f"inputs rotated over {n_sets} sets"}
+
+
 def bench_act_quant(fp8bs, dev, stream, peaks, args):
     """Activation quantizer alone on [16384, 7168] with 0.5% outlier channels
     x100, alternating between two seeded inputs (470 MB > L2)."""
@@ -474,7 +532,7 @@ def run_ours(args, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
-    parts = {"all": ("step", "act_quant", "norm_quant", "gemm2", "moe", "e2e")}.get(
+    parts = {"all": ("step", "act_quant", "norm_quant", "fused", "gemm2", "moe", "e2e")}.get(
         args.part, (args.part,))
 
     result = {}
@@ -502,6 +560,9 @@ def run_ours(args, world):
         torch.cuda.empty_cache()
     if "norm_quant" in parts:
         result["norm_quant"] = bench_norm_quant(fp8bs, dev, stream, peaks, args)
+        torch.cuda.empty_cache()
+    if "fused" in parts:
+        result["fused_act_quant_gemm"] = bench_fused(fp8bs, dev, stream, peaks, args)
         torch.cuda.empty_cache()
     if "gemm2" in parts:
         result["gemm_4096x7168x2048"] = bench_gemm2(fp8bs, dev, stream, peaks, args)
@@ -604,7 +665,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--part", choices=["all", "step", "act_quant", "norm_quant", "gemm2", "moe", "e2e"],
+    ap.add_argument("--part", choices=["all", "step", "act_quant", "norm_quant", "fused", "gemm2", "moe",
+                                       "e2e"],
                     default="all", help="which measurements to run (profiling uses one)")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle CPU baseline")
     args = ap.parse_args()

@@ -278,6 +278,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
                      : "memory");
 }
 
+// Makes this thread's generic-proxy writes to shared memory visible to later
+// async-proxy reads (tensor-core operands, bulk copies) ordered after it.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

@@ -50,6 +50,7 @@
 #include <cudaTypedefs.h>
 
 #include "fp8bs_device.cuh"
+#include "fp8bs_e4m3.cuh"
 #include "fp8bs_host.h"
 
 namespace fp8bs {
@@ -57,33 +58,51 @@ namespace {
 
 constexpr int BM = 128;   // output rows per CTA (TMEM lanes)
 constexpr int BK = 128;   // K chunk = one scale group
-constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 512;
 constexpr int kEpiRowBytes = 80;
 constexpr int kProducerRegs = 56;
-constexpr int kEpilogueRegs = 224;
 
-template <int kCtas, int kBN>
+// kFused: A arrives as bf16 and is quantized to E4M3 1x128 tiles inside the
+// kernel (four converter warps, warps 12-15) instead of being read as
+// pre-quantized codes; the rest of the pipeline is unchanged.
+template <int kCtas, int kBN, bool kFused = false>
 struct Cfg {
     static constexpr int kBRows = kBN / kCtas;            // W rows staged per CTA
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = kBRows * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (192 * 1024) / kStageBytes;   // 4, 6 or 8
+    // The fused kernel gives 48 KB to its bf16 ring, so it keeps 3 stages.
+    static constexpr int kStages = kFused ? 3 : (192 * 1024) / kStageBytes;   // 4, 6 or 8
     static constexpr int kSlots = kTmemCols / kBN;        // TMEM accumulator slots
     static constexpr int kCols = kBN / 2;                 // columns per promotion thread
     static constexpr int kTileRows = BM * kCtas;          // output rows per tile
+    static constexpr int kTileN = kBN;                    // output columns per tile
     static constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * kCtas, kBN);
+    static constexpr int kThreads = kFused ? 512 : 384;
+    // Registers per thread after setmaxnreg: warps 0-3 (and the converters)
+    // shrink, the promotion warps grow; the sums equal the launch budget
+    // (65536 per CTA).
+    static constexpr int kEpilogueRegs = kFused ? 200 : 224;
+    // bf16 A ring (fused only): half chunks of 128 rows x 64 K (16 KB).
+    static constexpr int kHalfStages = kFused ? 3 : 1;
+    static constexpr int kHalfBytes = kFused ? BM * 64 * 2 : 16;
+    static constexpr int kSaRing = kFused ? 8 : 1;       // per-chunk activation scales in flight
 };
 
-template <int kCtas, int kBN>
+template <int kCtas, int kBN, bool kFused = false>
 struct __align__(1024) Smem {
-    using C = Cfg<kCtas, kBN>;
+    using C = Cfg<kCtas, kBN, kFused>;
     uint8_t a[C::kStages][C::kABytes];
     uint8_t b[C::kStages][C::kBBytes];
-    uint64_t full[C::kStages];            // even CTA: both CTAs' TMA bytes
+    uint8_t abf[C::kHalfStages][C::kHalfBytes];   // fused: bf16 A halves, 128-byte swizzled
+    uint64_t full[C::kStages];            // even CTA: both CTAs' TMA bytes (+ converter warps)
     uint64_t empty[C::kStages];
+    uint64_t bfull[C::kHalfStages];       // fused: bf16 half landed
+    uint64_t bempty[C::kHalfStages];      // fused: 4 converter warps done with it
+    uint64_t sa_full[C::kSaRing];         // fused: 4 converter warps wrote the chunk's scales
+    uint64_t sa_empty[C::kSaRing];        // fused: 8 promotion warps read them
+    float sa_ring[C::kSaRing][kFused ? BM : 1];
     uint64_t tmem_full[C::kSlots];
     uint64_t tmem_empty[C::kSlots];       // even CTA: 8 arrivals per CTA of the pair
     uint64_t drain;
@@ -97,11 +116,19 @@ struct __align__(1024) Smem {
     int tile_start[kMaxExperts + 1];   // first tile index of each expert
     int row_start[kMaxExperts + 1];    // copy of expert_offsets
 };
-template <int kCtas, int kBN>
+template <int kCtas, int kBN, bool kFused = false>
 constexpr size_t smem_bytes()
 {
-    return sizeof(Smem<kCtas, kBN>) + 1024;   // + alignment slack
+    return sizeof(Smem<kCtas, kBN, kFused>) + 1024;   // + alignment slack
 }
+
+// 227 KB: the dynamic shared memory a CTA may opt into on sm_100-class GPUs.
+constexpr size_t kMaxSmemPerCta = 232448;
+static_assert(smem_bytes<1, 256>() <= kMaxSmemPerCta, "shared memory");
+static_assert(smem_bytes<1, 128>() <= kMaxSmemPerCta, "shared memory");
+static_assert(smem_bytes<2, 256>() <= kMaxSmemPerCta, "shared memory");
+static_assert(smem_bytes<2, 128>() <= kMaxSmemPerCta, "shared memory");
+static_assert(smem_bytes<1, 256, true>() <= kMaxSmemPerCta, "shared memory");
 
 struct Params {
     const float* sa;          // [rows, KB]
@@ -130,10 +157,11 @@ struct Tile {
 // Tile t of the launch: the expert e with tile_start[e] <= t < tile_start[e+1]
 // (binary search; a dense launch is one expert covering all rows), then the
 // m-tile and n-tile within that expert, m-tiles fastest.
-template <int kCtas, int kBN>
-__device__ __forceinline__ Tile decode_tile(const Smem<kCtas, kBN>& sm, const Params& p, int t)
+template <typename S>
+__device__ __forceinline__ Tile decode_tile(const S& sm, const Params& p, int t)
 {
-    constexpr int kTileRows = Cfg<kCtas, kBN>::kTileRows;
+    constexpr int kTileRows = S::C::kTileRows;
+    constexpr int kBN = S::C::kTileN;
     int lo = 0, hi = p.E;   // invariant: tile_start[lo] <= t < tile_start[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -186,10 +214,10 @@ __device__ __forceinline__ Segments work_of(const Params& p, int num_tiles, int 
 // Warp 3: copy and validate expert_offsets (a dense launch uses {0, M}),
 // then build tile_start[] (exclusive prefix sum of m-tiles x n-tiles per
 // expert).
-template <int kCtas, int kBN>
-__device__ void build_expert_table(Smem<kCtas, kBN>& sm, const Params& p, int lane)
+template <typename S>
+__device__ void build_expert_table(S& sm, const Params& p, int lane)
 {
-    constexpr int kTileRows = Cfg<kCtas, kBN>::kTileRows;
+    constexpr int kTileRows = S::C::kTileRows;
     bool ok = true;
     for (int base = 0; base <= p.E; base += 32) {
         const int i = base + lane;
@@ -235,13 +263,14 @@ __device__ void build_expert_table(Smem<kCtas, kBN>& sm, const Params& p, int la
     }
 }
 
-template <int kCtas, int kBN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kCtas, int kBN, bool kFused = false>
+__global__ void __launch_bounds__(Cfg<kCtas, kBN, kFused>::kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p)
 {
-    using C = Cfg<kCtas, kBN>;
-    using S = Smem<kCtas, kBN>;
+    using C = Cfg<kCtas, kBN, kFused>;
+    using S = Smem<kCtas, kBN, kFused>;
+    static_assert(!kFused || (kCtas == 1 && kBN == 256), "the fused kernel is the 128 x 256 tile");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     S& sm = *reinterpret_cast<S*>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
@@ -257,8 +286,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_addr(&sm.full[s]), 1);
+            mbar_init(smem_addr(&sm.full[s]), kFused ? 5 : 1);   // fused: + 4 converter warps
             mbar_init(smem_addr(&sm.empty[s]), 1);
+        }
+        if constexpr (kFused) {
+            for (int h = 0; h < C::kHalfStages; ++h) {
+                mbar_init(smem_addr(&sm.bfull[h]), 1);
+                mbar_init(smem_addr(&sm.bempty[h]), 4);
+            }
+            for (int i = 0; i < C::kSaRing; ++i) {
+                mbar_init(smem_addr(&sm.sa_full[i]), 4);
+                mbar_init(smem_addr(&sm.sa_empty[i]), 8);
+            }
         }
         for (int b = 0; b < C::kSlots; ++b) {
             mbar_init(smem_addr(&sm.tmem_full[b]), 1);
@@ -288,7 +327,80 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     const int num_tiles = sm.num_tiles;
     volatile int* abort_flag = &sm.abort;
 
-    if (warp < 4) {
+    if (kFused && warp >= 12) {
+        regs_dec<kProducerRegs>();
+        // -------------------------------------------------- A converters
+        // Warp cw handles rows 32 pass + 8 cw + lane/4 (pass = 0..3) of the
+        // chunk; the lane quad t = lane & 3 of a row holds its 16-byte
+        // pieces 2t, 2t+1 of both bf16 halves (K 16t..16t+15 and
+        // 64+16t..64+16t+15), so the row's amax is a quad max-exchange and
+        // its codes are the 16-byte E4M3 pieces t and 4+t of the row.
+        // Scale and codes are those of the 1x128 activation quantizer
+        // (same codec); codes go to the stage's A tile in the MMA's
+        // 128-byte-swizzled layout, scales to the ring the promotion warps
+        // read.
+        const int cw = warp - 12;
+        const int qrow = lane >> 2;
+        const int t4 = lane & 3;
+        uint32_t chunk = 0;
+        bool ok = true;
+        Segments work = work_of(p, num_tiles, unit, n_units);
+        int t, k0, k1;
+        while (ok && work.next(t, k0, k1)) {
+            for (int kb = k0; kb < k1; ++kb, ++chunk) {
+                const uint32_t hs0 = (2 * chunk) % C::kHalfStages, hs1 = (2 * chunk + 1) % C::kHalfStages;
+                const uint32_t hp0 = ((2 * chunk) / C::kHalfStages) & 1u;
+                const uint32_t hp1 = ((2 * chunk + 1) / C::kHalfStages) & 1u;
+                const uint32_t s = chunk % C::kStages, sp = (chunk / C::kStages) & 1u;
+                const uint32_t ring = chunk % C::kSaRing, rp = (chunk / C::kSaRing) & 1u;
+                const bool ready = mbar_wait(smem_addr(&sm.bfull[hs0]), hp0, abort_flag, p.err) &&
+                                   mbar_wait(smem_addr(&sm.bfull[hs1]), hp1, abort_flag, p.err) &&
+                                   mbar_wait(smem_addr(&sm.empty[s]), sp ^ 1u, abort_flag, p.err) &&
+                                   mbar_wait(smem_addr(&sm.sa_empty[ring]), rp ^ 1u, abort_flag, p.err);
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* half0 = sm.abf[hs0];
+                const uint8_t* half1 = sm.abf[hs1];
+                uint8_t* adst = sm.a[s];
+#pragma unroll 1
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int r = pass * 32 + cw * 8 + qrow;   // row of the tile
+                    const int sw = r & 7;                       // 128-byte swizzle phase of the row
+                    uint4 v[4];
+                    v[0] = *reinterpret_cast<const uint4*>(half0 + r * 128 + (((2 * t4) ^ sw) << 4));
+                    v[1] = *reinterpret_cast<const uint4*>(half0 + r * 128 + (((2 * t4 + 1) ^ sw) << 4));
+                    v[2] = *reinterpret_cast<const uint4*>(half1 + r * 128 + (((2 * t4) ^ sw) << 4));
+                    v[3] = *reinterpret_cast<const uint4*>(half1 + r * 128 + (((2 * t4 + 1) ^ sw) << 4));
+                    uint32_t m = absmax_words(v, 4);
+                    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                    const Divider d = make_divider(bf16_bits_to_f32(m));
+                    const bool fast = d.r != 0.0f;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint2 lo = fast ? quantize8_fast_fp(v[2 * h], d) : quantize8(v[2 * h], d);
+                        const uint2 hi = fast ? quantize8_fast_fp(v[2 * h + 1], d) : quantize8(v[2 * h + 1], d);
+                        const int jf = 4 * h + t4;                  // 16-byte piece of the E4M3 row
+                        *reinterpret_cast<uint4*>(adst + r * 128 + ((jf ^ sw) << 4)) =
+                            make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                    if (t4 == 0)
+                        sm.sa_ring[ring][r] = d.s;
+                }
+                // The codes are read by the tensor cores (async proxy).
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_addr(&sm.full[s]));
+                    mbar_arrive(smem_addr(&sm.bempty[hs0]));
+                    mbar_arrive(smem_addr(&sm.bempty[hs1]));
+                    mbar_arrive(smem_addr(&sm.sa_full[ring]));
+                }
+            }
+        }
+    } else if (warp < 4) {
         regs_dec<kProducerRegs>();
         if (warp == 0) {
             // ---------------------------------------------------- TMA producer
@@ -303,6 +415,28 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 const int32_t a_row = static_cast<int32_t>(tile.m0) + static_cast<int32_t>(rank) * BM;
                 const int32_t b_row = tile.b_row0 + static_cast<int32_t>(rank) * C::kBRows;
                 for (int kb = k0; kb < k1; ++kb, ++chunk) {
+                    if constexpr (kFused) {
+                        // The chunk's bf16 A as two 64-wide halves (128 B
+                        // rows, 128-byte swizzle) for the converter warps.
+                        for (uint32_t h = 0; h < 2; ++h) {
+                            const uint32_t hc = 2 * chunk + h;
+                            const uint32_t hs = hc % C::kHalfStages;
+                            const uint32_t hph = (hc / C::kHalfStages) & 1u;
+                            const bool free_ = mbar_wait(smem_addr(&sm.bempty[hs]), hph ^ 1u, abort_flag, p.err);
+                            if (!__all_sync(0xFFFFFFFFu, free_)) {
+                                ok = false;
+                                break;
+                            }
+                            if (elect_one()) {
+                                const uint32_t bar = smem_addr(&sm.bfull[hs]);
+                                mbar_arrive_expect_tx(bar, C::kHalfBytes);
+                                tma_load_2d(smem_addr(sm.abf[hs]), &map_a, bar, kb * BK + 64 * h, a_row);
+                            }
+                            __syncwarp();
+                        }
+                        if (!ok)
+                            break;
+                    }
                     const bool ready = mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err);
                     if (!__all_sync(0xFFFFFFFFu, ready)) {
                         ok = false;
@@ -310,7 +444,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     }
                     const uint32_t full = smem_addr(&sm.full[s]);
                     if (elect_one()) {
-                        if (kCtas == 1) {
+                        if (kFused) {
+                            // A comes from the converter warps (their 4 arrivals).
+                            mbar_arrive_expect_tx(full, C::kBBytes);
+                            tma_load_2d(smem_addr(sm.b[s]), &map_b, full, kb * BK, b_row);
+                        } else if (kCtas == 1) {
                             mbar_arrive_expect_tx(full, C::kStageBytes);
                             tma_load_2d(smem_addr(sm.a[s]), &map_a, full, kb * BK, a_row);
                             tma_load_2d(smem_addr(sm.b[s]), &map_b, full, kb * BK, b_row);
@@ -332,17 +470,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
             if (!ok) {
                 // Let the copies already issued land before the CTA exits.
-                if (kCtas == 1 || leader) {
+                if (kFused || (kCtas == 2 && !leader)) {
+                    // The fused kernel's stage barriers also count converter
+                    // arrivals, and the odd CTA's copies complete on its
+                    // partner's barrier: give the copies a fixed time.
+                    const unsigned long long t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) {
+                    }
+                } else {
                     const uint32_t first = chunk > C::kStages ? chunk - C::kStages : 0;
                     for (uint32_t c = first; c < chunk; ++c)
                         mbar_wait_drain(smem_addr(&sm.full[c % C::kStages]),
                                         (c / C::kStages) & 1u, kWaitLimitNs, p.err);
-                } else {
-                    // The odd CTA's copies complete on its partner's barrier,
-                    // which it cannot wait on: give them a fixed time.
-                    const unsigned long long t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) {
-                    }
                 }
             }
         } else if (warp == 1 && leader) {
@@ -404,7 +543,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             __syncwarp();
         }
     } else {
-        regs_inc<kEpilogueRegs>();
+        regs_inc<C::kEpilogueRegs>();
         // ------------------------------------------------------- promotion
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;      // output columns kCols*half .. +kCols-1
@@ -501,13 +640,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // rotated as chunks are consumed. Rows past the end read the last
             // row; their results are never stored.
             const int64_t srow = min(tile.m0 + rank * BM + r, p.rows - 1);
-            const float* sa_row = p.sa + srow * p.KB;
+            const float* sa_row = kFused ? nullptr : p.sa + srow * p.KB;
             const float* sw_row =
                 p.sw + (static_cast<int64_t>(tile.expert) * p.NB + min(n_col / 128, p.NB - 1)) * p.KB;
             auto load4 = [&](int kb0, float4& a4, float4& w4) {
                 const int last = p.KB - 1;
-                a4 = make_float4(__ldg(sa_row + min(kb0, last)), __ldg(sa_row + min(kb0 + 1, last)),
-                                 __ldg(sa_row + min(kb0 + 2, last)), __ldg(sa_row + min(kb0 + 3, last)));
+                if constexpr (kFused)
+                    a4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);   // activation scales come from the ring
+                else
+                    a4 = make_float4(__ldg(sa_row + min(kb0, last)), __ldg(sa_row + min(kb0 + 1, last)),
+                                     __ldg(sa_row + min(kb0 + 2, last)), __ldg(sa_row + min(kb0 + 3, last)));
                 w4 = make_float4(__ldg(sw_row + min(kb0, last)), __ldg(sw_row + min(kb0 + 1, last)),
                                  __ldg(sw_row + min(kb0 + 2, last)), __ldg(sw_row + min(kb0 + 3, last)));
             };
@@ -524,7 +666,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     cs = make_float4(na.x * nw.x, na.y * nw.y, na.z * nw.z, na.w * nw.w);
                     load4(kb + 4, na, nw);
                 }
-                if (!promote(chunk, cs.x, acc)) {
+                float scale = cs.x;
+                if constexpr (kFused) {
+                    // The converter warps' scale of this row and chunk; the
+                    // product is formed in the same order as sa * sw above.
+                    const uint32_t ring = chunk % C::kSaRing;
+                    const bool got = mbar_wait(smem_addr(&sm.sa_full[ring]), (chunk / C::kSaRing) & 1u,
+                                               abort_flag, p.err);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const float sa_v = sm.sa_ring[ring][r];
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_addr(&sm.sa_empty[ring]));
+                    scale = sa_v * cs.x;
+                }
+                if (!promote(chunk, scale, acc)) {
                     ok = false;
                     break;
                 }
@@ -641,19 +800,38 @@ bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
     return r == CUDA_SUCCESS;
 }
 
+// bf16 activations [rows, K] with row stride ld elements, as boxes of 64 (K)
+// x 128 rows (128-byte rows), 128-byte swizzled: the two halves of a K chunk.
+bool encode_bf16_halves(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld)
+{
+    auto enc = get_encoder();
+    if (enc == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BM)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Per device and shape: the dynamic shared-memory opt-in and the number of
 // work units (CTAs, or CTA pairs, which must share a GPC) resident at once.
-template <int kCtas, int kBN>
+template <int kCtas, int kBN, bool kFused = false>
 fp8bs_status configure_once(int device, int sm_count, int* max_units)
 {
+    constexpr int kThreads = Cfg<kCtas, kBN, kFused>::kThreads;
     static std::mutex mu;
     static int units[64] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64)
         return FP8BS_ERR_CUDA;
     if (units[device] == 0) {
-        const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
-        const size_t smem = smem_bytes<kCtas, kBN>();
+        const auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused>;
+        const size_t smem = smem_bytes<kCtas, kBN, kFused>();
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess) {
             cudaGetLastError();
@@ -690,11 +868,14 @@ fp8bs_status configure_once(int device, int sm_count, int* max_units)
 // computed on the device from the expert table (a dense launch is one
 // expert); the grid is the resident maximum, capped by an upper bound of the
 // tiles.
-template <int kCtas, int kBN>
-fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
-                    int64_t K, cudaStream_t stream)
+// kFused: a points at bf16 activations with row stride lda (elements);
+// otherwise at E4M3 codes with row stride K.
+template <int kCtas, int kBN, bool kFused = false>
+fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
+                    int64_t K, cudaStream_t stream, int64_t lda = 0)
 {
-    using C = Cfg<kCtas, kBN>;
+    using C = Cfg<kCtas, kBN, kFused>;
+    constexpr int kThreads = C::kThreads;
     DeviceInfo info;
     fp8bs_status st = require_sm103(&info);
     if (st != FP8BS_OK)
@@ -710,20 +891,21 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     memset(&map_a, 0, sizeof map_a);
     memset(&map_b, 0, sizeof map_b);
     if (K > 0) {
-        if (!encode_operand(&map_a, qa, rows, K, BM) ||
-            !encode_operand(&map_b, qw, w_rows, K, C::kBRows))
+        const bool a_ok = kFused ? encode_bf16_halves(&map_a, a, rows, K, lda)
+                                 : encode_operand(&map_a, a, rows, K, BM);
+        if (!a_ok || !encode_operand(&map_b, qw, w_rows, K, C::kBRows))
             return FP8BS_ERR_CUDA;
     }
     int max_units = 0;
-    st = configure_once<kCtas, kBN>(info.device, info.sm_count, &max_units);
+    st = configure_once<kCtas, kBN, kFused>(info.device, info.sm_count, &max_units);
     if (st != FP8BS_OK)
         return st;
-    const auto kernel = fp8_gemm_kernel<kCtas, kBN>;
+    const auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused>;
     const int units = static_cast<int>(tile_bound < max_units ? tile_bound : max_units);
     if (units <= 0)
         return FP8BS_OK;
     if (kCtas == 1) {
-        kernel<<<units, kThreads, smem_bytes<kCtas, kBN>(), stream>>>(map_a, map_b, p);
+        kernel<<<units, kThreads, smem_bytes<kCtas, kBN, kFused>(), stream>>>(map_a, map_b, p);
         return launch_status();
     }
     cudaLaunchConfig_t cfg = {};
@@ -734,7 +916,7 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * units);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<kCtas, kBN>();
+    cfg.dynamicSmemBytes = smem_bytes<kCtas, kBN, kFused>();
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -745,12 +927,15 @@ fp8bs_status launch(const uint8_t* qa, int64_t rows, const uint8_t* qw, int64_t 
     return FP8BS_OK;
 }
 
+// sa == nullptr is accepted when need_sa is false (the fused kernels make
+// the activation scales themselves).
 fp8bs_status check_common(const void* qa, const float* sa, const void* qw, const float* sw,
                           const void* c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
-                          int64_t ldc)
+                          int64_t ldc, bool need_sa = true)
 {
     // With K == 0 the operands are empty and never read; only C is written.
-    if (c == nullptr || (K > 0 && (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr)))
+    if (c == nullptr ||
+        (K > 0 && (qa == nullptr || (need_sa && sa == nullptr) || qw == nullptr || sw == nullptr)))
         return FP8BS_ERR_INVALID_ARG;
     if (out_dtype != FP8BS_OUT_F32 && out_dtype != FP8BS_OUT_BF16)
         return FP8BS_ERR_INVALID_ARG;
@@ -889,4 +1074,63 @@ extern "C" fp8bs_status fp8bs_grouped_gemm(const uint8_t* qa, const float* sa,
 {
     return fp8bs_grouped_gemm_tiled(qa, sa, expert_offsets, E, total_M, qw, sw, c, out_dtype, N, K,
                                     ldc, FP8BS_TILE_AUTO, stream);
+}
+
+// Row stride checks of a bf16 activation operand of the fused kernels.
+static fp8bs_status check_bf16_act(const void* a, int64_t lda, int64_t K)
+{
+    if (K > 0 && (a == nullptr || lda < K || (lda * 2) % 16 != 0 || !aligned16(a)))
+        return FP8BS_ERR_INVALID_ARG;
+    return FP8BS_OK;
+}
+
+extern "C" fp8bs_status fp8bs_gemm_bf16_act(const void* a, int64_t lda, const uint8_t* qw,
+                                            const float* sw, void* c, fp8bs_out_dtype out_dtype,
+                                            int64_t M, int64_t N, int64_t K, int64_t ldc,
+                                            fp8bs_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % BK != 0 || N % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    fp8bs_status st = check_bf16_act(a, lda, K);
+    if (st != FP8BS_OK)
+        return st;
+    st = check_common(a, nullptr, qw, sw, c, out_dtype, N, K, ldc, false);
+    if (st != FP8BS_OK)
+        return st;
+    if (M > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
+    const Params p = make_params(nullptr, sw, c, out_dtype, M, N, K, ldc, nullptr, 1);
+    return launch<1, 256, true>(a, M, qw, N, p, K, reinterpret_cast<cudaStream_t>(stream), lda);
+}
+
+extern "C" fp8bs_status fp8bs_grouped_gemm_bf16_act(const void* a, int64_t lda,
+                                                    const int32_t* expert_offsets, int32_t E,
+                                                    int64_t total_M, const uint8_t* qw,
+                                                    const float* sw, void* c,
+                                                    fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
+                                                    int64_t ldc, fp8bs_stream_t stream)
+{
+    if (E < 1 || total_M < 0 || N < 0 || K < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (E > kMaxExperts || K % BK != 0 || N % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    if (total_M == 0 || N == 0)
+        return FP8BS_OK;
+    if (expert_offsets == nullptr || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_bf16_act(a, lda, K);
+    if (st != FP8BS_OK)
+        return st;
+    st = check_common(a, nullptr, qw, sw, c, out_dtype, N, K, ldc, false);
+    if (st != FP8BS_OK)
+        return st;
+    if (total_M > 0x7FFFFFFF || static_cast<int64_t>(E) * N > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
+    const Params p = make_params(nullptr, sw, c, out_dtype, total_M, N, K, ldc, expert_offsets, E);
+    return launch<1, 256, true>(a, total_M, qw, static_cast<int64_t>(E) * N, p, K,
+                                reinterpret_cast<cudaStream_t>(stream), lda);
 }

@@ -62,6 +62,11 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_norm_quantize_act_1x128.argtypes = [vp, i64, i64, i64, vp, vp, ctypes.c_int,
                                                     ctypes.c_float, vp, i64, f32p, f32p, f32p, vp]
         L.fp8bs_norm_quantize_act_1x128.restype = st
+        L.fp8bs_gemm_bf16_act.argtypes = [vp, i64, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64, vp]
+        L.fp8bs_gemm_bf16_act.restype = st
+        L.fp8bs_grouped_gemm_bf16_act.argtypes = [vp, i64, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
+                                                  i64, i64, i64, vp]
+        L.fp8bs_grouped_gemm_bf16_act.restype = st
         L.fp8bs_status_string.argtypes = [ctypes.c_int]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
@@ -187,6 +192,32 @@ def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None, tile=TILE
                lib().fp8bs_grouped_gemm_tiled(*args, int(tile), _stream(stream)))
 
 
+def fp8bs_gemm_bf16_act(a, qw, sw, c, stream=None):
+    """C = (1x128-quantized a) @ dequant(qw, sw)^T with the activation
+    quantization inside the GEMM kernel; a is bf16 [M, K]."""
+    M, K = a.shape
+    N = qw.shape[0]
+    assert a.dtype == torch.bfloat16
+    for t in (qw, sw):
+        assert t.is_contiguous()
+    _check("fp8bs_gemm_bf16_act", lib().fp8bs_gemm_bf16_act(
+        _ptr(a), _row_stride(a), _ptr(_u8(qw)), _ptr(sw), _ptr(c), _out_dtype(c), M, N, K,
+        _row_stride(c), _stream(stream)))
+
+
+def fp8bs_grouped_gemm_bf16_act(a, expert_offsets, qw, sw, c, stream=None):
+    """Grouped GEMM with the activation quantization inside the kernel."""
+    total_M, K = a.shape
+    E, N, _ = qw.shape
+    assert a.dtype == torch.bfloat16
+    assert expert_offsets.dtype == torch.int32 and expert_offsets.numel() == E + 1
+    for t in (qw, sw, expert_offsets):
+        assert t.is_contiguous()
+    _check("fp8bs_grouped_gemm_bf16_act", lib().fp8bs_grouped_gemm_bf16_act(
+        _ptr(a), _row_stride(a), _ptr(expert_offsets), E, total_M, _ptr(_u8(qw)), _ptr(sw), _ptr(c),
+        _out_dtype(c), N, K, _row_stride(c), _stream(stream)))
+
+
 def fp8bs_last_device_error(stream=None) -> int:
     """Synchronizes the stream; returns (and clears) the device error status."""
     return lib().fp8bs_last_device_error(_stream(stream))
@@ -225,6 +256,18 @@ def quantize_weight(w: torch.Tensor, stream=None):
 def gemm(qa, sa, qw, sw, out_dtype=torch.bfloat16, stream=None, tile=TILE_AUTO):
     c = torch.empty((qa.shape[0], qw.shape[0]), dtype=out_dtype, device=qa.device)
     fp8bs_gemm(qa, sa, qw, sw, c, stream, tile)
+    return c
+
+
+def gemm_bf16_act(a, qw, sw, out_dtype=torch.bfloat16, stream=None):
+    c = torch.empty((a.shape[0], qw.shape[0]), dtype=out_dtype, device=a.device)
+    fp8bs_gemm_bf16_act(a, qw, sw, c, stream)
+    return c
+
+
+def grouped_gemm_bf16_act(a, expert_offsets, qw, sw, out_dtype=torch.bfloat16, stream=None):
+    c = torch.zeros((a.shape[0], qw.shape[1]), dtype=out_dtype, device=a.device)
+    fp8bs_grouped_gemm_bf16_act(a, expert_offsets, qw, sw, c, stream)
     return c
 
 

@@ -207,6 +207,30 @@ fp8bs_status fp8bs_grouped_gemm_tiled(const uint8_t *qa, const float *sa,
                                       fp8bs_out_dtype out_dtype, int64_t N, int64_t K, int64_t ldc,
                                       fp8bs_tile tile, fp8bs_stream_t stream);
 
+/*
+ * The same GEMMs with the activation quantization fused in: A is given as
+ * bf16 [M, K] (row stride lda elements, 16-byte aligned rows) and each
+ * 1x128 tile is quantized inside the GEMM kernel -- loaded by TMA, scaled
+ * and cast in shared memory, handed to the tensor cores -- so the E4M3 copy
+ * of A and its scales never go to memory. This emulates in software the
+ * fusion of the FP8 cast with the TMA load that "How I Improved My Deepseek
+ * In In The Future" asks of future hardware (paragraph of hardware
+ * suggestions). The codes and scales used are exactly those of
+ * fp8bs_quantize_act_1x128, and the result is bit-identical to
+ * fp8bs_quantize_act_1x128 followed by fp8bs_gemm_tiled /
+ * fp8bs_grouped_gemm_tiled with FP8BS_TILE_128x256. W, its scales, C and the
+ * remaining arguments are as in fp8bs_gemm / fp8bs_grouped_gemm.
+ */
+fp8bs_status fp8bs_gemm_bf16_act(const void *a, int64_t lda, const uint8_t *qw, const float *sw,
+                                 void *c, fp8bs_out_dtype out_dtype, int64_t M, int64_t N,
+                                 int64_t K, int64_t ldc, fp8bs_stream_t stream);
+
+fp8bs_status fp8bs_grouped_gemm_bf16_act(const void *a, int64_t lda,
+                                         const int32_t *expert_offsets, int32_t E,
+                                         int64_t total_M, const uint8_t *qw, const float *sw,
+                                         void *c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
+                                         int64_t ldc, fp8bs_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *fp8bs_status_string(fp8bs_status status);
 

@@ -8,7 +8,8 @@ from fp8_fine_grained_17_b300 import fp8bs
 
 EXPECTED = {"fp8bs_quantize_act_1x128", "fp8bs_quantize_weight_128x128", "fp8bs_gemm",
             "fp8bs_grouped_gemm", "fp8bs_gemm_tiled", "fp8bs_grouped_gemm_tiled",
-            "fp8bs_norm_quantize_act_1x128", "fp8bs_status_string", "fp8bs_last_device_error"}
+            "fp8bs_norm_quantize_act_1x128", "fp8bs_gemm_bf16_act", "fp8bs_grouped_gemm_bf16_act",
+            "fp8bs_status_string", "fp8bs_last_device_error"}
 
 
 def test_header_declares_the_boundary():
@@ -98,3 +99,21 @@ def test_norm_argument_checks():
     assert f(P, 4, 128, 128, P, P + 8, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # beta align
     assert f(P, 4, 128, 128, P, None, R, 1e-6, P, 128, P, P + 2, None, None) == fp8bs.ERR_INVALID_ARG  # mean align
     assert f(P, 4, 128, 120, P, None, R, 1e-6, P, 128, P, None, None, None) == fp8bs.ERR_INVALID_ARG  # ldx < K
+
+
+def test_bf16_act_gemm_argument_checks():
+    f = fp8bs.lib().fp8bs_gemm_bf16_act
+    assert f(P, 128, P, P, P, 1, 0, 256, 128, 256, None) == fp8bs.OK                   # M = 0
+    assert f(P, 128, P, P, P, 1, -1, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 128, P, P, P, 1, 4, 200, 128, 200, None) == fp8bs.ERR_UNSUPPORTED     # N % 128
+    assert f(P, 100, P, P, P, 1, 4, 256, 100, 256, None) == fp8bs.ERR_UNSUPPORTED     # K % 128
+    assert f(P, 120, P, P, P, 1, 4, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG     # lda < K
+    assert f(P, 132, P, P, P, 1, 4, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG     # row not 16B
+    assert f(P + 8, 128, P, P, P, 1, 4, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG  # misaligned
+    assert f(None, 128, P, P, P, 1, 4, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 128, P, None, P, 1, 4, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG  # sw
+    g = fp8bs.lib().fp8bs_grouped_gemm_bf16_act
+    assert g(P, 128, P, 2, 0, P, P, P, 1, 256, 128, 256, None) == fp8bs.OK             # no rows
+    assert g(P, 128, P, 0, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
+    assert g(P, 128, P, 513, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_UNSUPPORTED
+    assert g(P, 128, P + 2, 2, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
