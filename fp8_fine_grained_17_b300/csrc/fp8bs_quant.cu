@@ -69,45 +69,53 @@ __device__ __forceinline__ void quantize_quad(const uint4 (&v)[4][4], const bool
 // kContiguous: rows back to back (ld == K), group g starts at element 128 g.
 constexpr int kActThreads = 256;
 
+// One batch of the register path: the 32 groups starting at group `base`
+// (one per lane; the warp's lane quads take four groups each).
+template <bool kContiguous>
+__device__ __forceinline__ void act_regs_batch(int64_t base, const uint16_t* __restrict__ x, int64_t ldx,
+                                               uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
+                                               int64_t groups_per_row, int64_t total_groups)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 3;
+    const int quad_base = lane & ~3;
+    uint4 v[4][4];
+    uint8_t* qdst[4];
+    bool valid[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t g = base + quad_base + u;
+        valid[u] = g < total_groups;
+        int64_t xo, qo;
+        if (kContiguous) {
+            xo = valid[u] ? g * 128 : 0;
+            qo = xo;
+        } else {
+            const int64_t row = valid[u] ? g / groups_per_row : 0;
+            const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
+            xo = row * ldx + col;
+            qo = row * ldq + col;
+        }
+        qdst[u] = q + qo;
+        const uint4* src = reinterpret_cast<const uint4*>(x + xo) + t;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t my_g = base + lane;   // scale is [M, K/128] row-major: index = g
+    quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, 0);
+}
+
 template <bool kContiguous>
 __global__ void __launch_bounds__(kActThreads)
 quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
                          int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
                          int64_t total_groups)
 {
-    const int lane = threadIdx.x & 31;
-    const int t = lane & 3;
-    const int quad_base = lane & ~3;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kActThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kActThreads) >> 5;
-
-    for (int64_t base = warp * 32; base < total_groups; base += n_warps * 32) {
-        uint4 v[4][4];
-        uint8_t* qdst[4];
-        bool valid[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t g = base + quad_base + u;
-            valid[u] = g < total_groups;
-            int64_t xo, qo;
-            if (kContiguous) {
-                xo = valid[u] ? g * 128 : 0;
-                qo = xo;
-            } else {
-                const int64_t row = valid[u] ? g / groups_per_row : 0;
-                const int64_t col = valid[u] ? (g - row * groups_per_row) * 128 : 0;
-                xo = row * ldx + col;
-                qo = row * ldq + col;
-            }
-            qdst[u] = q + qo;
-            const uint4* src = reinterpret_cast<const uint4*>(x + xo) + t;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
-        }
-        const int64_t my_g = base + lane;   // scale is [M, K/128] row-major: index = g
-        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, 0);
-    }
+    for (int64_t base = warp * 32; base < total_groups; base += n_warps * 32)
+        act_regs_batch<kContiguous>(base, x, ldx, q, ldq, scale, groups_per_row, total_groups);
 }
 
 // Large contiguous inputs (ld == K, at least kTmaMinGroups groups): the
@@ -230,16 +238,12 @@ quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__
 // ---------------------------------------------------------------------------
 constexpr int kWThreads = 256;
 
-__global__ void __launch_bounds__(kWThreads)
-quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
-                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
-                       int64_t groups_per_row)
+__device__ __forceinline__ void weight_block(int64_t kb, int64_t nb, const uint16_t* __restrict__ w, int64_t N,
+                                             int64_t ldw, uint8_t* __restrict__ q, int64_t ldq,
+                                             float* __restrict__ scale, int64_t groups_per_row,
+                                             uint32_t* warp_max, Divider* block_div)
 {
-    __shared__ uint32_t warp_max[kWThreads / 32];
-    __shared__ Divider block_div;
     const int t = threadIdx.x;
-    const int64_t kb = blockIdx.x;
-    const int64_t nb = blockIdx.y;
     const int chunk = t & 15;
     const int64_t col = kb * 128 + chunk * 8;
 
@@ -260,16 +264,52 @@ quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
         for (int i = 1; i < kWThreads / 32; ++i)
             a = max(a, warp_max[i]);
         const Divider d = make_divider(bf16_bits_to_f32(a));
-        block_div = d;
+        *block_div = d;
         scale[nb * groups_per_row + kb] = d.s;
     }
     __syncthreads();
-    const Divider d = block_div;
+    const Divider d = *block_div;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t n = nb * 128 + i * 16 + (t >> 4);
         if (n < N)
             __stcs(reinterpret_cast<uint2*>(q + n * ldq + col), quantize8(v[i], d));
+    }
+}
+
+__global__ void __launch_bounds__(kWThreads)
+quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
+                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
+                       int64_t groups_per_row)
+{
+    __shared__ uint32_t warp_max[kWThreads / 32];
+    __shared__ Divider block_div;
+    weight_block(blockIdx.x, blockIdx.y, w, N, ldw, q, ldq, scale, groups_per_row, warp_max, &block_div);
+}
+
+// Both quantizers in one launch (a step's activation and weight
+// quantizations are independent): blocks [0, act_blocks) each quantize one
+// 256-group batch of the activations through the register path, the others
+// one 128x128 weight block each, so the two share one wave of the GPU.
+static_assert(kActThreads == kWThreads, "one block size for both roles");
+
+template <bool kContiguous>
+__global__ void __launch_bounds__(kWThreads)
+quantize_pair_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ qx, int64_t ldqx,
+                     float* __restrict__ sx, int64_t x_groups_per_row, int64_t x_groups, int64_t act_blocks,
+                     const uint16_t* __restrict__ w, int64_t N, int64_t ldw, uint8_t* __restrict__ qw,
+                     int64_t ldqw, float* __restrict__ sw, int64_t w_groups_per_row)
+{
+    __shared__ uint32_t warp_max[kWThreads / 32];
+    __shared__ Divider block_div;
+    const int64_t b = blockIdx.x;
+    if (b < act_blocks) {
+        act_regs_batch<kContiguous>((b * (kActThreads / 32) + (threadIdx.x >> 5)) * 32, x, ldx, qx, ldqx, sx,
+                                    x_groups_per_row, x_groups);
+    } else {
+        const int64_t wb = b - act_blocks;
+        weight_block(wb % w_groups_per_row, wb / w_groups_per_row, w, N, ldw, qw, ldqw, sw,
+                     w_groups_per_row, warp_max, &block_div);
     }
 }
 
@@ -393,5 +433,50 @@ extern "C" fp8bs_status fp8bs_quantize_weight_128x128(const void* w, int64_t N, 
     const dim3 grid(static_cast<unsigned>(G), static_cast<unsigned>(NB));
     quantize_weight_kernel<<<grid, kWThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(w), N, ldw, q, ldq, scale, G);
+    return launch_status();
+}
+
+extern "C" fp8bs_status fp8bs_quantize_act_and_weight(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                                      uint8_t* qx, int64_t ldqx, float* sx,
+                                                      const void* w, int64_t N, int64_t Kw,
+                                                      int64_t ldw, uint8_t* qw, int64_t ldqw,
+                                                      float* sw, fp8bs_stream_t stream)
+{
+    if (M < 0 || K < 0 || N < 0 || Kw < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % 128 != 0 || Kw % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    const bool do_x = M > 0 && K > 0, do_w = N > 0 && Kw > 0;
+    if (do_x && (x == nullptr || qx == nullptr || sx == nullptr || ldx < K || ldqx < K ||
+                 (ldx * 2) % 16 != 0 || ldqx % 16 != 0 || !aligned16(x) || !aligned16(qx) ||
+                 (reinterpret_cast<uintptr_t>(sx) & 3u) != 0))
+        return FP8BS_ERR_INVALID_ARG;
+    if (do_w && (w == nullptr || qw == nullptr || sw == nullptr || ldw < Kw || ldqw < Kw ||
+                 (ldw * 2) % 16 != 0 || ldqw % 16 != 0 || !aligned16(w) || !aligned16(qw) ||
+                 (reinterpret_cast<uintptr_t>(sw) & 3u) != 0))
+        return FP8BS_ERR_INVALID_ARG;
+    if (!do_x && !do_w)
+        return FP8BS_OK;
+    const int64_t x_groups = do_x ? M * (K / 128) : 0;
+    const int64_t act_blocks = (x_groups + kActThreads - 1) / kActThreads;   // 256 groups per block
+    const int64_t w_gpr = do_w ? Kw / 128 : 1;
+    const int64_t w_blocks = do_w ? ((N + 127) / 128) * w_gpr : 0;
+    if (act_blocks + w_blocks > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
+    DeviceInfo info;
+    const fp8bs_status st = require_sm103(&info);
+    if (st != FP8BS_OK)
+        return st;
+    const dim3 grid(static_cast<unsigned>(act_blocks + w_blocks));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const auto* xb = static_cast<const uint16_t*>(x);
+    const auto* wb = static_cast<const uint16_t*>(w);
+    const int64_t x_gpr = do_x ? K / 128 : 1;
+    if (!do_x || (ldx == K && ldqx == K))
+        quantize_pair_kernel<true><<<grid, kWThreads, 0, s>>>(xb, ldx, qx, ldqx, sx, x_gpr, x_groups, act_blocks,
+                                                              wb, N, ldw, qw, ldqw, sw, w_gpr);
+    else
+        quantize_pair_kernel<false><<<grid, kWThreads, 0, s>>>(xb, ldx, qx, ldqx, sx, x_gpr, x_groups, act_blocks,
+                                                               wb, N, ldw, qw, ldqw, sw, w_gpr);
     return launch_status();
 }

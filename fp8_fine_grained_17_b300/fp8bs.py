@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_grouped_gemm_bf16_act.argtypes = [vp, i64, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
                                                   i64, i64, i64, vp]
         L.fp8bs_grouped_gemm_bf16_act.restype = st
+        L.fp8bs_quantize_act_and_weight.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp, i64, i64, i64,
+                                                    vp, i64, f32p, vp]
+        L.fp8bs_quantize_act_and_weight.restype = st
         L.fp8bs_status_string.argtypes = [ctypes.c_int]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
@@ -151,6 +154,19 @@ def fp8bs_norm_quantize_act_1x128(x: torch.Tensor, gamma: torch.Tensor, beta, ki
     _check("fp8bs_norm_quantize_act_1x128", lib().fp8bs_norm_quantize_act_1x128(
         _ptr(x), M, K, _row_stride(x), _ptr(gamma), _ptr(beta), int(kind), float(eps),
         _ptr(q8), _row_stride(q8), _ptr(scale), _ptr(mean), _ptr(rstd), _stream(stream)))
+
+
+def fp8bs_quantize_act_and_weight(x, qx, sx, w, qw, sw, stream=None):
+    """Both quantizers in one launch (same results as the two calls)."""
+    M, K = x.shape
+    N, Kw = w.shape
+    assert x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16
+    assert sx.dtype == torch.float32 and sw.dtype == torch.float32
+    assert sx.is_contiguous() and sw.is_contiguous()
+    qx8, qw8 = _u8(qx), _u8(qw)
+    _check("fp8bs_quantize_act_and_weight", lib().fp8bs_quantize_act_and_weight(
+        _ptr(x), M, K, _row_stride(x), _ptr(qx8), _row_stride(qx8), _ptr(sx),
+        _ptr(w), N, Kw, _row_stride(w), _ptr(qw8), _row_stride(qw8), _ptr(sw), _stream(stream)))
 
 
 def _out_dtype(c: torch.Tensor) -> int:

@@ -95,6 +95,20 @@ fp8bs_status fp8bs_quantize_act_1x128(const void *x, int64_t M, int64_t K, int64
                                       uint8_t *q, int64_t ldq, float *scale,
                                       fp8bs_stream_t stream);
 
+/*
+ * Both quantizations of an FP8 linear layer in one launch: the activations
+ * x [M, K] in 1x128 tiles (as fp8bs_quantize_act_1x128) and the weights
+ * w [N, Kw] in 128x128 blocks (as fp8bs_quantize_weight_128x128). The two are
+ * independent; one launch lets them share the GPU instead of running back to
+ * back. Codes and scales are bit-identical to the two separate calls; the
+ * arguments, layouts and checks are theirs. Either part may be empty
+ * (M == 0 or N == 0).
+ */
+fp8bs_status fp8bs_quantize_act_and_weight(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                           uint8_t *qx, int64_t ldqx, float *sx, const void *w,
+                                           int64_t N, int64_t Kw, int64_t ldw, uint8_t *qw,
+                                           int64_t ldqw, float *sw, fp8bs_stream_t stream);
+
 /* Normalization applied by fp8bs_norm_quantize_act_1x128. */
 typedef enum { FP8BS_NORM_RMS = 0, FP8BS_NORM_LAYER = 1 } fp8bs_norm_kind;
 

@@ -9,6 +9,7 @@ from fp8_fine_grained_17_b300 import fp8bs
 EXPECTED = {"fp8bs_quantize_act_1x128", "fp8bs_quantize_weight_128x128", "fp8bs_gemm",
             "fp8bs_grouped_gemm", "fp8bs_gemm_tiled", "fp8bs_grouped_gemm_tiled",
             "fp8bs_norm_quantize_act_1x128", "fp8bs_gemm_bf16_act", "fp8bs_grouped_gemm_bf16_act",
+            "fp8bs_quantize_act_and_weight",
             "fp8bs_status_string", "fp8bs_last_device_error"}
 
 
@@ -117,3 +118,15 @@ def test_bf16_act_gemm_argument_checks():
     assert g(P, 128, P, 0, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
     assert g(P, 128, P, 513, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_UNSUPPORTED
     assert g(P, 128, P + 2, 2, 10, P, P, P, 1, 256, 128, 256, None) == fp8bs.ERR_INVALID_ARG
+
+
+def test_pair_quantize_argument_checks():
+    f = fp8bs.lib().fp8bs_quantize_act_and_weight
+    assert f(P, 0, 128, 128, P, 128, P, P, 0, 128, 128, P, 128, P, None) == fp8bs.OK       # both empty
+    assert f(P, -1, 128, 128, P, 128, P, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 100, 128, P, 128, P, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_UNSUPPORTED
+    assert f(P, 4, 128, 128, P, 128, P, P, 4, 130, 130, P, 130, P, None) == fp8bs.ERR_UNSUPPORTED
+    assert f(None, 4, 128, 128, P, 128, P, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 128, 128, P, 128, P, P, 4, 128, 128, None, 128, P, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 128, 120, P, 128, P, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+    assert f(P, 4, 128, 128, P, 128, P + 2, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG

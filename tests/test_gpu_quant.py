@@ -119,3 +119,34 @@ def test_exhaustive_amax_x_pairs(orc):
         assert torch.all(qp[rows.shape[0]:] == 0) and torch.all(sp[rows.shape[0]:] == 1.0)
     pool.shutdown()
     assert total > 1.07e9
+
+
+@pytest.mark.parametrize("M,K,N,Kw,strided", [
+    (4096, 7168, 4096, 7168, False), (1, 128, 300, 256, False), (37, 384, 0, 128, False),
+    (0, 128, 129, 512, False), (257, 1152, 640, 896, True),
+])
+def test_pair_quantizer_matches_separate(orc, M, K, N, Kw, strided):
+    """One launch of both quantizers: codes and scales bit-identical to the
+    oracle (and so to the separate kernels)."""
+    rng = np.random.default_rng(M + K + N + Kw)
+    a_bits, _ = wl.activations(rng, M, K, 100.0)
+    w_bits = wl.weights(rng, N, Kw)
+    pad = 64 if strided else 0
+    xs = torch.zeros((M, K + pad), dtype=torch.bfloat16, device="cuda")
+    xs[:, :K] = wl.bits_to_torch(a_bits).cuda()
+    ws = torch.zeros((N, Kw + pad), dtype=torch.bfloat16, device="cuda")
+    ws[:, :Kw] = wl.bits_to_torch(w_bits).cuda()
+    qxs = torch.zeros((M, K + pad), dtype=torch.uint8, device="cuda")
+    qws = torch.zeros((N, Kw + pad), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    sw = torch.empty(((N + 127) // 128, Kw // 128), dtype=torch.float32, device="cuda")
+    fp8bs.fp8bs_quantize_act_and_weight(xs[:, :K], qxs[:, :K], sx, ws[:, :Kw], qws[:, :Kw], sw)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    if M:
+        q_o, s_o = orc.quantize_act_1x128(a_bits)
+        check_codes(qxs[:, :K], sx, q_o, s_o)
+    if N:
+        q_o, s_o = orc.quantize_weight_128x128(w_bits)
+        check_codes(qws[:, :Kw], sw, q_o, s_o)
+    if pad:
+        assert torch.all(qxs[:, K:] == 0).item() and torch.all(qws[:, Kw:] == 0).item()
