@@ -116,6 +116,23 @@ float fp8o_group_scale(float amax)
     return amax / 448.0f;
 }
 
+/* Power-of-two scale (the scale mode Blackwell's UE8M0 microscaling formats
+ * can hold): the smallest s = 2^e, -127 <= e <= 127, with amax / s <= 448,
+ * i.e. 2^e >= amax / 448 as real numbers; s = 1 when amax = 0. Found by a
+ * plain upward search over e with the exact comparison amax <= 448 * 2^e
+ * (both sides exact in binary64). */
+float fp8o_group_scale_pow2(float amax)
+{
+    int e = -127;
+    if (amax == 0.0f)
+        return 1.0f;
+    while (e < 127 && (double)amax > ldexp(448.0, e))
+        ++e;
+    return ldexpf(1.0f, e);
+}
+
+typedef float (*fp8o_scale_fn)(float amax);
+
 /* One element: q = E4M3(x / s), with x / s a correctly rounded binary32
  * division followed by the E4M3 rounding (two roundings, by definition). */
 uint8_t fp8o_quantize_value(float x, float s)
@@ -127,8 +144,8 @@ uint8_t fp8o_quantize_value(float x, float s)
 /* Activations, 1x128 tiles: x is bf16 [M, K] with row stride ldx (elements);
  * q is [M, K] with row stride ldq (bytes); scale is [M, K/128] row-major.
  * K must be a multiple of 128. */
-void fp8o_quantize_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                             uint8_t *q, int64_t ldq, float *scale)
+static void fp8o_act_tiles(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q,
+                           int64_t ldq, float *scale, fp8o_scale_fn group_scale)
 {
     int64_t G = K / 128;
     for (int64_t m = 0; m < M; ++m) {
@@ -141,7 +158,7 @@ void fp8o_quantize_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ld
                 if (v > amax)
                     amax = v;
             }
-            s = fp8o_group_scale(amax);
+            s = group_scale(amax);
             scale[m * G + g] = s;
             for (int k = 0; k < 128; ++k)
                 qg[k] = fp8o_quantize_value(fp8o_bf16_to_f32(xg[k]), s);
@@ -149,12 +166,25 @@ void fp8o_quantize_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ld
     }
 }
 
+void fp8o_quantize_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t *q, int64_t ldq, float *scale)
+{
+    fp8o_act_tiles(x, M, K, ldx, q, ldq, scale, fp8o_group_scale);
+}
+
+/* The same tiles with power-of-two scales. */
+void fp8o_quantize_act_1x128_pow2(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t *q, int64_t ldq, float *scale)
+{
+    fp8o_act_tiles(x, M, K, ldx, q, ldq, scale, fp8o_group_scale_pow2);
+}
+
 /* Weights, 128x128 blocks: w is bf16 [N, K] (output channel x input channel)
  * with row stride ldw; q is [N, K] with row stride ldq; scale is
  * [ceil(N/128), K/128] row-major. The last row block is partial when N is
  * not a multiple of 128; only rows that exist enter its amax. */
-void fp8o_quantize_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
-                                  uint8_t *q, int64_t ldq, float *scale)
+static void fp8o_weight_blocks(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q,
+                               int64_t ldq, float *scale, fp8o_scale_fn group_scale)
 {
     int64_t G = K / 128;
     int64_t NB = (N + 127) / 128;
@@ -168,7 +198,7 @@ void fp8o_quantize_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64
                     if (v > amax)
                         amax = v;
                 }
-            s = fp8o_group_scale(amax);
+            s = group_scale(amax);
             scale[nb * G + g] = s;
             for (int64_t n = nb * 128; n < n_end; ++n)
                 for (int k = 0; k < 128; ++k)
@@ -178,8 +208,32 @@ void fp8o_quantize_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64
     }
 }
 
+void fp8o_quantize_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                  uint8_t *q, int64_t ldq, float *scale)
+{
+    fp8o_weight_blocks(w, N, K, ldw, q, ldq, scale, fp8o_group_scale);
+}
+
+/* The same blocks with power-of-two scales. */
+void fp8o_quantize_weight_128x128_pow2(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                       uint8_t *q, int64_t ldq, float *scale)
+{
+    fp8o_weight_blocks(w, N, K, ldw, q, ldq, scale, fp8o_group_scale_pow2);
+}
+
 /* Element-wise form used by exhaustive sweeps: codes of x[i] under the
- * scale of amax[i]. */
+ * scale of amax[i] (power-of-two scales when pow2 != 0). */
+void fp8o_quantize_pairs_mode(const uint16_t *amax_bf16, const uint16_t *x_bf16, int64_t n,
+                              uint8_t *q, float *scale, int pow2)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fp8o_bf16_to_f32(amax_bf16[i]);
+        float s = pow2 ? fp8o_group_scale_pow2(a) : fp8o_group_scale(a);
+        scale[i] = s;
+        q[i] = fp8o_quantize_value(fp8o_bf16_to_f32(x_bf16[i]), s);
+    }
+}
+
 void fp8o_quantize_pairs(const uint16_t *amax_bf16, const uint16_t *x_bf16, int64_t n,
                          uint8_t *q, float *scale)
 {

@@ -26,6 +26,10 @@ What it computes, and the passage each step follows:
   post, paragraph on quantizing before the MoE up-projection for FP8 Fprop).
 * Acceptance bound: |C_gpu - C_or| <= 2e-5 * sum_k |A_hat W_hat| + 1e-6, plus
   2^-8 |C_or| for a bf16 output (statement of the problem).
+* Power-of-two scale mode (the scales Blackwell's UE8M0 microscaling
+  formats hold; the pages point to Blackwell microscaling as the direction
+  of FP8 hardware): s = the smallest power of two with amax / s <= 448, by a
+  plain search in ``fp8bs_oracle.c``; codes and GEMM as above.
 * Normalization fused with the 1x128 cast (RMSNorm or LayerNorm, bf16
   output, then the activation quantizer): "How I Improved My Deepseek In In
   The Future", paragraph of hardware suggestions (fusion of layer
@@ -83,6 +87,14 @@ def lib() -> ctypes.CDLL:
         L.fp8o_quantize_weight_128x128.argtypes = [u16p, i64, i64, i64, u8p, i64, f32p]
         L.fp8o_quantize_pairs.restype = None
         L.fp8o_quantize_pairs.argtypes = [u16p, u16p, i64, u8p, f32p]
+        L.fp8o_group_scale_pow2.restype = ctypes.c_float
+        L.fp8o_group_scale_pow2.argtypes = [ctypes.c_float]
+        L.fp8o_quantize_act_1x128_pow2.restype = None
+        L.fp8o_quantize_act_1x128_pow2.argtypes = [u16p, i64, i64, i64, u8p, i64, f32p]
+        L.fp8o_quantize_weight_128x128_pow2.restype = None
+        L.fp8o_quantize_weight_128x128_pow2.argtypes = [u16p, i64, i64, i64, u8p, i64, f32p]
+        L.fp8o_quantize_pairs_mode.restype = None
+        L.fp8o_quantize_pairs_mode.argtypes = [u16p, u16p, i64, u8p, f32p, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -121,20 +133,21 @@ def quantize_value(x: float, s: float) -> int:
 # Quantizers. Inputs are bf16 bit patterns held as uint16 arrays.
 # ---------------------------------------------------------------------------
 
-def quantize_act_1x128(x_bits: np.ndarray):
-    """x_bits: uint16 [M, K] (bf16 patterns) -> (q uint8 [M, K], s float32 [M, K/128])."""
+def quantize_act_1x128(x_bits: np.ndarray, pow2: bool = False):
+    """x_bits: uint16 [M, K] (bf16 patterns) -> (q uint8 [M, K], s float32 [M, K/128]).
+    pow2: power-of-two scales (group_scale_pow2) instead of amax / 448."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     M, K = x_bits.shape
     assert K % 128 == 0
     q = np.empty((M, K), dtype=np.uint8)
     s = np.empty((M, K // 128), dtype=np.float32)
     if M and K:
-        lib().fp8o_quantize_act_1x128(_ptr(x_bits, ctypes.c_uint16), M, K, K,
-                                      _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
+        fn = lib().fp8o_quantize_act_1x128_pow2 if pow2 else lib().fp8o_quantize_act_1x128
+        fn(_ptr(x_bits, ctypes.c_uint16), M, K, K, _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
     return q, s
 
 
-def quantize_weight_128x128(w_bits: np.ndarray):
+def quantize_weight_128x128(w_bits: np.ndarray, pow2: bool = False):
     """w_bits: uint16 [N, K] -> (q uint8 [N, K], s float32 [ceil(N/128), K/128])."""
     w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
     N, K = w_bits.shape
@@ -142,12 +155,16 @@ def quantize_weight_128x128(w_bits: np.ndarray):
     q = np.empty((N, K), dtype=np.uint8)
     s = np.empty(((N + 127) // 128, K // 128), dtype=np.float32)
     if N and K:
-        lib().fp8o_quantize_weight_128x128(_ptr(w_bits, ctypes.c_uint16), N, K, K,
-                                           _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
+        fn = lib().fp8o_quantize_weight_128x128_pow2 if pow2 else lib().fp8o_quantize_weight_128x128
+        fn(_ptr(w_bits, ctypes.c_uint16), N, K, K, _ptr(q, ctypes.c_uint8), K, _ptr(s, ctypes.c_float))
     return q, s
 
 
-def quantize_pairs(amax_bits: np.ndarray, x_bits: np.ndarray):
+def group_scale_pow2(amax: float) -> np.float32:
+    return np.float32(lib().fp8o_group_scale_pow2(float(np.float32(amax))))
+
+
+def quantize_pairs(amax_bits: np.ndarray, x_bits: np.ndarray, pow2: bool = False):
     """Codes of x under the scale of amax, element by element."""
     amax_bits = np.ascontiguousarray(amax_bits, dtype=np.uint16).ravel()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16).ravel()
@@ -155,8 +172,8 @@ def quantize_pairs(amax_bits: np.ndarray, x_bits: np.ndarray):
     q = np.empty(n, dtype=np.uint8)
     s = np.empty(n, dtype=np.float32)
     if n:
-        lib().fp8o_quantize_pairs(_ptr(amax_bits, ctypes.c_uint16), _ptr(x_bits, ctypes.c_uint16),
-                                  n, _ptr(q, ctypes.c_uint8), _ptr(s, ctypes.c_float))
+        lib().fp8o_quantize_pairs_mode(_ptr(amax_bits, ctypes.c_uint16), _ptr(x_bits, ctypes.c_uint16),
+                                       n, _ptr(q, ctypes.c_uint8), _ptr(s, ctypes.c_float), int(pow2))
     return q, s
 
 

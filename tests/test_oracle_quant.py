@@ -178,3 +178,61 @@ def test_pairs_match_groups(orc):
     qp, sp = orc.quantize_pairs(amax, x)
     assert np.array_equal(qp.reshape(3, 128), q)
     assert np.array_equal(sp.reshape(3, 128)[:, 0], s[:, 0])
+
+
+# ---------------------------------------------------------------- power-of-two scales
+
+@pytest.mark.parametrize("amax,want", [
+    (0.0, 1.0),              # all-zero group: s = 1
+    (448.0, 1.0),            # 448 / 1 = 448 is allowed
+    (449.0, 2.0),            # 449 / 1 > 448, 449 / 2 <= 448
+    (1.0, 2.0 ** -8),        # 1 / 2^-8 = 256 <= 448 < 512
+    (896.0, 2.0),
+    (897.0, 4.0),
+    (1.75, 2.0 ** -8),       # 1.75 * 256 = 448 exactly
+    (1.7578125, 2.0 ** -7),  # next bf16 above 1.75: 450 > 448
+])
+def test_pow2_scale_hand_values(orc, amax, want):
+    assert orc.group_scale_pow2(amax) == np.float32(want)
+
+
+def test_pow2_scale_every_bf16_amax(orc):
+    """For every positive finite bf16 amax: s is a power of two in
+    [2^-127, 2^127], amax / s <= 448, and s / 2 would exceed 448 unless s is
+    already the smallest allowed power (exact rational arithmetic)."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    amax = wl.bits_to_f32(bits).astype(np.float64)
+    s = np.array([orc.group_scale_pow2(a) for a in amax], dtype=np.float64)
+    mant, ex = np.frexp(s)
+    assert np.all(mant == 0.5)                      # exact powers of two
+    assert np.all((ex - 1 >= -127) & (ex - 1 <= 127))
+    assert np.all(amax <= 448.0 * s)                 # exact: s is 2^e, 448 = 7 * 2^6
+    smaller_ok = (ex - 1 > -127)
+    assert np.all(amax[smaller_ok] > 448.0 * (s[smaller_ok] / 2))
+
+
+def test_pow2_codes_are_nearest_grid(orc):
+    """With s = 2^e, x / s is exact, so every code is the nearest E4M3 value of
+    x / s (ties to even, saturating) -- checked by brute force on the grid."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((16, 256)) * np.exp(rng.uniform(-20, 20, (16, 1)))).astype(np.float32)
+    xb = wl.bf16_bits(x)
+    q, s = orc.quantize_act_1x128(xb, pow2=True)
+    table = orc.e4m3_table()
+    y = wl.bits_to_f32(xb).astype(np.float64) / np.repeat(s.astype(np.float64), 128, axis=1)
+    assert np.array_equal(q, _nearest_codes(table, y))
+    # The largest magnitude of each group has x / s in (224, 448], so its code
+    # (rounded to the E4M3 grid, spacing 16 in [128, 256)) is in [224, 448].
+    amax_code = np.abs(table[q]).reshape(16, 2, 128).max(axis=2)
+    assert np.all((amax_code >= 224.0) & (amax_code <= 448.0))
+
+
+def test_pow2_weight_blocks_match_single_groups(orc):
+    rng = np.random.default_rng(22)
+    w = wl.weights(rng, 200, 256)
+    q, s = orc.quantize_weight_128x128(w, pow2=True)
+    for nb in range(2):
+        rows = slice(128 * nb, min(128 * nb + 128, 200))
+        for kb in range(2):
+            blk = wl.bits_to_f32(w[rows, 128 * kb:128 * kb + 128])
+            assert s[nb, kb] == orc.group_scale_pow2(float(np.abs(blk).max()))
