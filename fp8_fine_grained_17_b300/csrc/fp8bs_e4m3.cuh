@@ -45,6 +45,36 @@ __device__ __forceinline__ Divider make_divider(float amax)
     return d;
 }
 
+// Power-of-two scale mode (the scales Blackwell's UE8M0 formats hold): s = 2^e
+// for the smallest e in [-127, 127] with amax / 2^e <= 448, taken exactly from
+// the bf16 pattern of amax (448 = 1.75 * 2^8, so e = E - 135 for a mantissa
+// <= 1.75 and E - 134 above it, E the biased exponent); s = 1 for amax = 0.
+// r = 2^-e exactly, so the fast quotient x * r is the exact (or, in the
+// binary32 subnormal range, correctly rounded) x / s.
+__device__ __forceinline__ Divider make_divider_pow2(uint32_t amax_bits)
+{
+    Divider d;
+    if (amax_bits == 0) {
+        d.s = 1.0f;
+        d.r = 1.0f;
+        return d;
+    }
+    const int eb = static_cast<int>((amax_bits >> 7) & 0xFFu);
+    const int mant = static_cast<int>(amax_bits & 0x7Fu);
+    int e = eb == 0 ? -127 : eb - 135 + (mant > 96 ? 1 : 0);
+    e = max(e, -127);
+    d.s = e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                    : __uint_as_float(0x00400000u);   // 2^-127 (subnormal)
+    d.r = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    return d;
+}
+
+// Scale and reciprocal of a group from the bf16 pattern of its amax.
+__device__ __forceinline__ Divider group_divider(uint32_t amax_bits, int pow2)
+{
+    return pow2 ? make_divider_pow2(amax_bits) : make_divider(__uint_as_float(amax_bits << 16));
+}
+
 // Largest |x| of a bf16 group fragment held as packed words, as the 16-bit
 // pattern of a non-negative bf16 (integer order = numeric order).
 __device__ __forceinline__ uint32_t absmax_words(const uint4* v, int n)

@@ -29,7 +29,7 @@ namespace {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void quantize_quad(const uint4 (&v)[4][4], const bool (&valid)[4],
                                               uint8_t* const (&qdst)[4], float* my_scale, int t,
-                                              int quad_base, int rot)
+                                              int quad_base, int rot, int pow2)
 {
     uint32_t m[4];
 #pragma unroll
@@ -46,7 +46,7 @@ __device__ __forceinline__ void quantize_quad(const uint4 (&v)[4][4], const bool
     const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, b0 ? k[0] : k[1], 1);
     const uint32_t mine = max(b0 ? k[1] : k[0], recv);
 
-    const Divider own = make_divider(bf16_bits_to_f32(mine));
+    const Divider own = group_divider(mine, pow2);
     if (my_scale != nullptr)
         *my_scale = own.s;
 
@@ -74,7 +74,7 @@ constexpr int kActThreads = 256;
 template <bool kContiguous>
 __device__ __forceinline__ void act_regs_batch(int64_t base, const uint16_t* __restrict__ x, int64_t ldx,
                                                uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
-                                               int64_t groups_per_row, int64_t total_groups)
+                                               int64_t groups_per_row, int64_t total_groups, int pow2)
 {
     const int lane = threadIdx.x & 31;
     const int t = lane & 3;
@@ -103,19 +103,19 @@ __device__ __forceinline__ void act_regs_batch(int64_t base, const uint16_t* __r
             v[u][j] = valid[u] ? __ldcs(src + 4 * j) : make_uint4(0, 0, 0, 0);
     }
     const int64_t my_g = base + lane;   // scale is [M, K/128] row-major: index = g
-    quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, 0);
+    quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, 0, pow2);
 }
 
 template <bool kContiguous>
 __global__ void __launch_bounds__(kActThreads)
 quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ q,
                          int64_t ldq, float* __restrict__ scale, int64_t groups_per_row,
-                         int64_t total_groups)
+                         int64_t total_groups, int pow2)
 {
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kActThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kActThreads) >> 5;
     for (int64_t base = warp * 32; base < total_groups; base += n_warps * 32)
-        act_regs_batch<kContiguous>(base, x, ldx, q, ldq, scale, groups_per_row, total_groups);
+        act_regs_batch<kContiguous>(base, x, ldx, q, ldq, scale, groups_per_row, total_groups, pow2);
 }
 
 // Large contiguous inputs (ld == K, at least kTmaMinGroups groups): the
@@ -142,7 +142,7 @@ constexpr size_t kActSmemBytes = sizeof(ActSmem) + 128;
 
 __global__ void __launch_bounds__(kTmaThreads)
 quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ q,
-                           float* __restrict__ scale, int64_t total_groups, unsigned int* err)
+                           float* __restrict__ scale, int64_t total_groups, unsigned int* err, int pow2)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -214,7 +214,7 @@ quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__
                                    : make_uint4(0, 0, 0, 0);
         }
         const int64_t my_g = g0 + warp * 32 + lane;
-        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, rot);
+        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, rot, pow2);
         __syncthreads();   // every thread is done with stage s
         if (threadIdx.x == 0) {
             const int64_t c2 = c + static_cast<int64_t>(kTmaStages) * gridDim.x;
@@ -241,7 +241,7 @@ constexpr int kWThreads = 256;
 __device__ __forceinline__ void weight_block(int64_t kb, int64_t nb, const uint16_t* __restrict__ w, int64_t N,
                                              int64_t ldw, uint8_t* __restrict__ q, int64_t ldq,
                                              float* __restrict__ scale, int64_t groups_per_row,
-                                             uint32_t* warp_max, Divider* block_div)
+                                             uint32_t* warp_max, Divider* block_div, int pow2)
 {
     const int t = threadIdx.x;
     const int chunk = t & 15;
@@ -263,7 +263,7 @@ __device__ __forceinline__ void weight_block(int64_t kb, int64_t nb, const uint1
 #pragma unroll
         for (int i = 1; i < kWThreads / 32; ++i)
             a = max(a, warp_max[i]);
-        const Divider d = make_divider(bf16_bits_to_f32(a));
+        const Divider d = group_divider(a, pow2);
         *block_div = d;
         scale[nb * groups_per_row + kb] = d.s;
     }
@@ -280,11 +280,12 @@ __device__ __forceinline__ void weight_block(int64_t kb, int64_t nb, const uint1
 __global__ void __launch_bounds__(kWThreads)
 quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t ldw,
                        uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scale,
-                       int64_t groups_per_row)
+                       int64_t groups_per_row, int pow2)
 {
     __shared__ uint32_t warp_max[kWThreads / 32];
     __shared__ Divider block_div;
-    weight_block(blockIdx.x, blockIdx.y, w, N, ldw, q, ldq, scale, groups_per_row, warp_max, &block_div);
+    weight_block(blockIdx.x, blockIdx.y, w, N, ldw, q, ldq, scale, groups_per_row, warp_max, &block_div,
+                 pow2);
 }
 
 // Both quantizers in one launch (a step's activation and weight
@@ -305,11 +306,11 @@ quantize_pair_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __res
     const int64_t b = blockIdx.x;
     if (b < act_blocks) {
         act_regs_batch<kContiguous>((b * (kActThreads / 32) + (threadIdx.x >> 5)) * 32, x, ldx, qx, ldqx, sx,
-                                    x_groups_per_row, x_groups);
+                                    x_groups_per_row, x_groups, 0);
     } else {
         const int64_t wb = b - act_blocks;
         weight_block(wb % w_groups_per_row, wb / w_groups_per_row, w, N, ldw, qw, ldqw, sw,
-                     w_groups_per_row, warp_max, &block_div);
+                     w_groups_per_row, warp_max, &block_div, 0);
     }
 }
 
@@ -334,9 +335,8 @@ int resident_blocks(Kernel kernel, int threads, size_t smem, int* cache)
 
 using namespace fp8bs;
 
-extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
-                                                 uint8_t* q, int64_t ldq, float* scale,
-                                                 fp8bs_stream_t stream)
+static fp8bs_status quantize_act_impl(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                      int64_t ldq, float* scale, fp8bs_stream_t stream, int pow2)
 {
     if (M < 0 || K < 0)
         return FP8BS_ERR_INVALID_ARG;
@@ -384,7 +384,7 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
         const int64_t chunks = (total + kTmaChunkGroups - 1) / kTmaChunkGroups;
         const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
         const int grid = static_cast<int>(chunks < full ? chunks : full);
-        quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err);
+        quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err, pow2);
     } else {
         const bool contiguous = ldx == K && ldq == K;
         static int per_sm[2] = {0, 0};
@@ -394,20 +394,33 @@ extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64
             resident_blocks(quantize_act_regs_kernel<true>, kActThreads, 0, &per_sm[1]);
             const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[1];
             quantize_act_regs_kernel<true><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
-                                             s>>>(xb, ldx, q, ldq, scale, G, total);
+                                             s>>>(xb, ldx, q, ldq, scale, G, total, pow2);
         } else {
             resident_blocks(quantize_act_regs_kernel<false>, kActThreads, 0, &per_sm[0]);
             const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[0];
             quantize_act_regs_kernel<false><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
-                                              s>>>(xb, ldx, q, ldq, scale, G, total);
+                                              s>>>(xb, ldx, q, ldq, scale, G, total, pow2);
         }
     }
     return launch_status();
 }
 
-extern "C" fp8bs_status fp8bs_quantize_weight_128x128(const void* w, int64_t N, int64_t K,
-                                                      int64_t ldw, uint8_t* q, int64_t ldq,
-                                                      float* scale, fp8bs_stream_t stream)
+extern "C" fp8bs_status fp8bs_quantize_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                                 uint8_t* q, int64_t ldq, float* scale,
+                                                 fp8bs_stream_t stream)
+{
+    return quantize_act_impl(x, M, K, ldx, q, ldq, scale, stream, 0);
+}
+
+extern "C" fp8bs_status fp8bs_quantize_act_1x128_pow2(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                                      uint8_t* q, int64_t ldq, float* scale,
+                                                      fp8bs_stream_t stream)
+{
+    return quantize_act_impl(x, M, K, ldx, q, ldq, scale, stream, 1);
+}
+
+static fp8bs_status quantize_weight_impl(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                         int64_t ldq, float* scale, fp8bs_stream_t stream, int pow2)
 {
     if (N < 0 || K < 0)
         return FP8BS_ERR_INVALID_ARG;
@@ -432,8 +445,22 @@ extern "C" fp8bs_status fp8bs_quantize_weight_128x128(const void* w, int64_t N, 
 
     const dim3 grid(static_cast<unsigned>(G), static_cast<unsigned>(NB));
     quantize_weight_kernel<<<grid, kWThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(w), N, ldw, q, ldq, scale, G);
+        static_cast<const uint16_t*>(w), N, ldw, q, ldq, scale, G, pow2);
     return launch_status();
+}
+
+extern "C" fp8bs_status fp8bs_quantize_weight_128x128(const void* w, int64_t N, int64_t K,
+                                                      int64_t ldw, uint8_t* q, int64_t ldq,
+                                                      float* scale, fp8bs_stream_t stream)
+{
+    return quantize_weight_impl(w, N, K, ldw, q, ldq, scale, stream, 0);
+}
+
+extern "C" fp8bs_status fp8bs_quantize_weight_128x128_pow2(const void* w, int64_t N, int64_t K,
+                                                           int64_t ldw, uint8_t* q, int64_t ldq,
+                                                           float* scale, fp8bs_stream_t stream)
+{
+    return quantize_weight_impl(w, N, K, ldw, q, ldq, scale, stream, 1);
 }
 
 extern "C" fp8bs_status fp8bs_quantize_act_and_weight(const void* x, int64_t M, int64_t K, int64_t ldx,

@@ -48,6 +48,10 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_quantize_act_1x128.restype = st
         L.fp8bs_quantize_weight_128x128.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp]
         L.fp8bs_quantize_weight_128x128.restype = st
+        L.fp8bs_quantize_act_1x128_pow2.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp]
+        L.fp8bs_quantize_act_1x128_pow2.restype = st
+        L.fp8bs_quantize_weight_128x128_pow2.argtypes = [vp, i64, i64, i64, vp, i64, f32p, vp]
+        L.fp8bs_quantize_weight_128x128_pow2.restype = st
         L.fp8bs_gemm.argtypes = [vp, f32p, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64, vp]
         L.fp8bs_gemm.restype = st
         L.fp8bs_grouped_gemm.argtypes = [vp, f32p, vp, i32, i64, vp, f32p, vp, ctypes.c_int,
@@ -120,21 +124,26 @@ def _u8(t: torch.Tensor) -> torch.Tensor:
 
 # ---------------------------------------------------------------- C entry points
 
-def fp8bs_quantize_act_1x128(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None):
-    """x bf16 [M, K] -> q e4m3/uint8 [M, K], scale fp32 [M, K/128] (contiguous)."""
+def fp8bs_quantize_act_1x128(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None,
+                             pow2: bool = False):
+    """x bf16 [M, K] -> q e4m3/uint8 [M, K], scale fp32 [M, K/128] (contiguous).
+    pow2: power-of-two scales (fp8bs_quantize_act_1x128_pow2)."""
     M, K = x.shape
     assert x.dtype == torch.bfloat16 and scale.dtype == torch.float32 and scale.is_contiguous()
     q8 = _u8(q)
-    _check("fp8bs_quantize_act_1x128", lib().fp8bs_quantize_act_1x128(
+    name = "fp8bs_quantize_act_1x128_pow2" if pow2 else "fp8bs_quantize_act_1x128"
+    _check(name, getattr(lib(), name)(
         _ptr(x), M, K, _row_stride(x), _ptr(q8), _row_stride(q8), _ptr(scale), _stream(stream)))
 
 
-def fp8bs_quantize_weight_128x128(w: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None):
+def fp8bs_quantize_weight_128x128(w: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None,
+                                  pow2: bool = False):
     """w bf16 [N, K] -> q [N, K], scale fp32 [ceil(N/128), K/128] (contiguous)."""
     N, K = w.shape
     assert w.dtype == torch.bfloat16 and scale.dtype == torch.float32 and scale.is_contiguous()
     q8 = _u8(q)
-    _check("fp8bs_quantize_weight_128x128", lib().fp8bs_quantize_weight_128x128(
+    name = "fp8bs_quantize_weight_128x128_pow2" if pow2 else "fp8bs_quantize_weight_128x128"
+    _check(name, getattr(lib(), name)(
         _ptr(w), N, K, _row_stride(w), _ptr(q8), _row_stride(q8), _ptr(scale), _stream(stream)))
 
 
@@ -241,11 +250,11 @@ def fp8bs_last_device_error(stream=None) -> int:
 
 # ------------------------------------------------------ allocating conveniences
 
-def quantize_act(x: torch.Tensor, stream=None):
+def quantize_act(x: torch.Tensor, stream=None, pow2: bool = False):
     M, K = x.shape
     q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     s = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
-    fp8bs_quantize_act_1x128(x, q, s, stream)
+    fp8bs_quantize_act_1x128(x, q, s, stream, pow2)
     return q, s
 
 
@@ -261,11 +270,11 @@ def norm_quantize_act(x: torch.Tensor, gamma: torch.Tensor, beta=None, kind: int
     return q, s, mean, rstd
 
 
-def quantize_weight(w: torch.Tensor, stream=None):
+def quantize_weight(w: torch.Tensor, stream=None, pow2: bool = False):
     N, K = w.shape
     q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
-    fp8bs_quantize_weight_128x128(w, q, s, stream)
+    fp8bs_quantize_weight_128x128(w, q, s, stream, pow2)
     return q, s
 
 

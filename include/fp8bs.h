@@ -96,6 +96,24 @@ fp8bs_status fp8bs_quantize_act_1x128(const void *x, int64_t M, int64_t K, int64
                                       fp8bs_stream_t stream);
 
 /*
+ * The two quantizers with power-of-two scales: s = 2^e for the smallest
+ * integer e in [-127, 127] with amax / 2^e <= 448 (s = 1 for an all-zero
+ * group), i.e. scales that the UE8M0 scale format of Blackwell's
+ * microscaling MMA can hold ("How I Improved My Deepseek In In The Future"
+ * points to Blackwell microscaling as the direction of FP8 hardware). Codes
+ * are E4M3(x / s) as before, now with an exact division. Layouts, checks and
+ * the GEMM that consumes the scales are unchanged; only the scale values
+ * differ (at most 2x larger than amax / 448, so codes use [224, 448] for each
+ * group's largest magnitude instead of exactly 448).
+ */
+fp8bs_status fp8bs_quantize_act_1x128_pow2(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                           uint8_t *q, int64_t ldq, float *scale,
+                                           fp8bs_stream_t stream);
+fp8bs_status fp8bs_quantize_weight_128x128_pow2(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                                uint8_t *q, int64_t ldq, float *scale,
+                                                fp8bs_stream_t stream);
+
+/*
  * Both quantizations of an FP8 linear layer in one launch: the activations
  * x [M, K] in 1x128 tiles (as fp8bs_quantize_act_1x128) and the weights
  * w [N, Kw] in 128x128 blocks (as fp8bs_quantize_weight_128x128). The two are

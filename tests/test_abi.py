@@ -9,7 +9,8 @@ from fp8_fine_grained_17_b300 import fp8bs
 EXPECTED = {"fp8bs_quantize_act_1x128", "fp8bs_quantize_weight_128x128", "fp8bs_gemm",
             "fp8bs_grouped_gemm", "fp8bs_gemm_tiled", "fp8bs_grouped_gemm_tiled",
             "fp8bs_norm_quantize_act_1x128", "fp8bs_gemm_bf16_act", "fp8bs_grouped_gemm_bf16_act",
-            "fp8bs_quantize_act_and_weight",
+            "fp8bs_quantize_act_and_weight", "fp8bs_quantize_act_1x128_pow2",
+            "fp8bs_quantize_weight_128x128_pow2",
             "fp8bs_status_string", "fp8bs_last_device_error"}
 
 
@@ -130,3 +131,13 @@ def test_pair_quantize_argument_checks():
     assert f(P, 4, 128, 128, P, 128, P, P, 4, 128, 128, None, 128, P, None) == fp8bs.ERR_INVALID_ARG
     assert f(P, 4, 128, 120, P, 128, P, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
     assert f(P, 4, 128, 128, P, 128, P + 2, P, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+
+
+def test_pow2_quantize_argument_checks():
+    L = fp8bs.lib()
+    for f in (L.fp8bs_quantize_act_1x128_pow2, L.fp8bs_quantize_weight_128x128_pow2):
+        assert f(P, 0, 128, 128, P, 128, P, None) == fp8bs.OK
+        assert f(P, -1, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+        assert f(P, 4, 100, 128, P, 128, P, None) == fp8bs.ERR_UNSUPPORTED
+        assert f(None, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG
+        assert f(P + 8, 4, 128, 128, P, 128, P, None) == fp8bs.ERR_INVALID_ARG

@@ -140,3 +140,33 @@ def test_tiles_bit_identical():
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
 
+
+
+def test_pow2_scales_gemm_parity_and_error(orc, capsys):
+    """The GEMM takes power-of-two scales unchanged (parity with the oracle),
+    and its error against the exact product of the bf16 inputs is compared
+    with that of the amax/448 scales on the same inputs (seeded; the numbers
+    are printed for the record)."""
+    M, N, K = 512, 1024, 2048
+    rng = np.random.default_rng(41)
+    a_bits, _ = wl.activations(rng, M, K, 50.0)
+    w_bits = wl.weights(rng, N, K)
+    exact = wl.bits_to_f32(a_bits).astype(np.float64) @ wl.bits_to_f32(w_bits).astype(np.float64).T
+    err = {}
+    for pow2 in (False, True):
+        qa, sa = fp8bs.quantize_act(wl.bits_to_torch(a_bits).cuda(), pow2=pow2)
+        qw, sw = fp8bs.quantize_weight(wl.bits_to_torch(w_bits).cuda(), pow2=pow2)
+        qa_o, sa_o = orc.quantize_act_1x128(a_bits, pow2=pow2)
+        qw_o, sw_o = orc.quantize_weight_128x128(w_bits, pow2=pow2)
+        check_codes(qa, sa, qa_o, sa_o)
+        check_codes(qw, sw, qw_o, sw_o)
+        c = fp8bs.gemm(qa, sa, qw, sw, torch.float32)
+        C_or, B = orc.gemm(qa_o, sa_o, qw_o, sw_o)
+        check_gemm(c, C_or, B, False)
+        got = c.cpu().numpy().astype(np.float64)
+        err[pow2] = float(np.linalg.norm(got - exact) / np.linalg.norm(exact))
+    with capsys.disabled():
+        print(f"\nrelative Frobenius error vs bf16 product: amax/448 scales {err[False]:.4e}, "
+              f"power-of-two scales {err[True]:.4e}")
+    assert err[False] < 0.05 and err[True] < 0.05
+    assert err[True] <= 1.5 * err[False]

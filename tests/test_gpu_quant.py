@@ -150,3 +150,53 @@ def test_pair_quantizer_matches_separate(orc, M, K, N, Kw, strided):
         check_codes(qws[:, :Kw], sw, q_o, s_o)
     if pad:
         assert torch.all(qxs[:, K:] == 0).item() and torch.all(qws[:, Kw:] == 0).item()
+
+
+
+# ---------------------------------------------------------------- power-of-two scales
+
+def _pow2_rows():
+    """One row per positive finite bf16 amax: [amax, -amax, -0, +0, then 124
+    seeded values with |x| <= amax spread over the binades below it]."""
+    rng = np.random.default_rng(31)
+    amax = np.arange(1, 0x7F80, dtype=np.uint16)
+    rows = np.zeros((amax.size, 128), dtype=np.uint16)
+    rows[:, 0] = amax
+    rows[:, 1] = amax | 0x8000
+    rows[:, 2] = 0x8000
+    frac = rng.random((amax.size, 124)) * np.exp2(-rng.integers(0, 40, (amax.size, 124)))
+    vals = wl.bits_to_f32(amax)[:, None] * frac.astype(np.float32)
+    vals *= np.where(rng.random(vals.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    b = wl.bf16_bits(vals)
+    mag = b & 0x7FFF
+    b = np.where(mag > amax[:, None], (b & 0x8000) | amax[:, None], b)   # rounding may pass amax
+    rows[:, 4:] = b
+    return rows
+
+
+def test_pow2_act_every_amax_both_paths(orc):
+    rows = _pow2_rows()
+    q_or, s_or = orc.quantize_act_1x128(rows, pow2=True)
+    x = to_dev_bf16(rows)
+    q, s = fp8bs.quantize_act(x, pow2=True)
+    check_codes(q, s, q_or, s_or)
+    padded = np.zeros((RING_MIN_GROUPS, 128), dtype=np.uint16)
+    padded[:rows.shape[0]] = rows
+    qp, sp = fp8bs.quantize_act(to_dev_bf16(padded), pow2=True)
+    check_codes(qp[:rows.shape[0]], sp[:rows.shape[0]], q_or, s_or)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (300, 256), (7168, 2048)])
+def test_pow2_weight_shapes(orc, N, K):
+    rng = np.random.default_rng(N + K + 1)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[N // 2, K // 3] = 3.0
+    bits = wl.bf16_bits(w)
+    q, s = fp8bs.quantize_weight(to_dev_bf16(bits), pow2=True)
+    check_codes(q, s, *orc.quantize_weight_128x128(bits, pow2=True))
+
+
+def test_pow2_act_full_workload(orc):
+    d = wl.cfg1(0)
+    q, s = fp8bs.quantize_act(to_dev_bf16(d.a_bits), pow2=True)
+    check_codes(q, s, *orc.quantize_act_1x128(d.a_bits, pow2=True))
