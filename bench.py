@@ -487,49 +487,52 @@ def bench_moe(fp8bs, dev, stream, peaks, args, n_tokens=wl.N_TOKENS):
 def bench_e2e(fp8bs, dev, stream, args):
     """Same step through the C entry points from pinned host buffers: every
     step copies A and W (bf16) host -> device, quantizes both (one launch),
-    runs the GEMM and copies C device -> host. W's upload runs on a second
-    stream beside A's; C's copy back runs on a third stream, so it overlaps
-    the next step's uploads (C alternates between two buffers)."""
+    runs the GEMM and copies C device -> host. Uploads run on their own
+    stream into alternating device buffers, so step i+1's uploads overlap
+    step i's kernels; C's copy back runs on a third stream (C alternates
+    between two buffers too)."""
     d = wl.cfg3(seed=0)
     a_h = wl.bits_to_torch(d.a_bits).pin_memory()
     w_h = wl.bits_to_torch(d.w_bits).pin_memory()
     c_h = [torch.empty((M3, N3), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    a = torch.empty((M3, K3), dtype=torch.bfloat16, device=dev)
-    w = torch.empty((N3, K3), dtype=torch.bfloat16, device=dev)
+    a = [torch.empty((M3, K3), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    w = [torch.empty((N3, K3), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     qa = torch.empty((M3, K3), dtype=torch.uint8, device=dev)
     sa = torch.empty((M3, K3 // 128), dtype=torch.float32, device=dev)
     qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
     sw = torch.empty((N3 // 128, K3 // 128), dtype=torch.float32, device=dev)
     c = [torch.empty((M3, N3), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    s_w = torch.cuda.Stream(dev)
+    s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
-    w_done = torch.cuda.Event()
-    gemm_done = torch.cuda.Event()
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
+    gemm_done = [torch.cuda.Event(), torch.cuda.Event()]
     out_done = [torch.cuda.Event(), torch.cuda.Event()]
-    for e in out_done:
-        e.record(s_out)
 
     def step(i):
         b = i & 1
-        with torch.cuda.stream(s_w):
-            s_w.wait_event(gemm_done)          # the previous step's quantizer has read w
-            w.copy_(w_h, non_blocking=True)
-            w_done.record(s_w)
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(consumed[b])       # step i-2's quantizer has read a[b], w[b]
+            a[b].copy_(a_h, non_blocking=True)
+            w[b].copy_(w_h, non_blocking=True)
+            in_ready[b].record(s_in)
         with torch.cuda.stream(stream):
-            a.copy_(a_h, non_blocking=True)
-            stream.wait_event(w_done)
-            fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, stream)
-            stream.wait_event(out_done[b])     # C[b]'s previous copy-out is done
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_done[b])     # step i-2's copy-out of C[b] is done
+            fp8bs.fp8bs_quantize_act_and_weight(a[b], qa, sa, w[b], qw, sw, stream)
+            consumed[b].record(stream)
             fp8bs.fp8bs_gemm(qa, sa, qw, sw, c[b], stream)
-            gemm_done.record(stream)
+            gemm_done[b].record(stream)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(gemm_done)
+            s_out.wait_event(gemm_done[b])
             c_h[b].copy_(c[b], non_blocking=True)
             out_done[b].record(s_out)
 
     def drain():
         stream.wait_event(out_done[0])
         stream.wait_event(out_done[1])
+        stream.wait_event(in_ready[0])
+        stream.wait_event(in_ready[1])
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -538,7 +541,7 @@ def bench_e2e(fp8bs, dev, stream, args):
     n = max(10, min(args.steps, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    s_w.wait_event(e0)
+    s_in.wait_event(e0)
     s_out.wait_event(e0)
     for i in range(n):
         step(i)
@@ -550,8 +553,9 @@ def bench_e2e(fp8bs, dev, stream, args):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": 2 * (M3 * K3 + N3 * K3), "d2h_bytes_per_step": 2 * M3 * N3,
             "ms_per_step": round(ms, 4), "steps": n,
-            "path": "pinned host A, W -> H2D (two streams) -> quantize A + W (one launch), GEMM -> "
-                    "D2H C (third stream, overlapping the next step's uploads)"}
+            "path": "pinned host A, W -> H2D (upload stream, alternating buffers) -> quantize A + W "
+                    "(one launch), GEMM -> D2H C (third stream); uploads and copy-back overlap "
+                    "the kernels of neighbouring steps"}
 
 
 def run_ours(args, world):

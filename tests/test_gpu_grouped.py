@@ -128,3 +128,28 @@ def test_grouped_every_tile(orc, tile):
     C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K),
                                s_o.reshape(E, N // 128, K // 128))
     check_gemm(c, C_or, B, False)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_grouped_max_experts(orc, fused):
+    """The largest expert count the library takes (512), most experts empty or
+    with a handful of rows, a few with several m-tiles; quantized operands
+    and, separately, the kernel with the activation quantization inside."""
+    rng = np.random.default_rng(77)
+    counts = rng.choice([0, 0, 1, 2, 3], size=512)
+    counts[[5, 300, 511]] = [130, 257, 64]
+    N, K = 256, 256
+    d = wl.moe(seed=77, N=N, K=K, counts=counts)
+    E = 512
+    qw, sw = _quant_experts(orc, d.w_bits, check=False)
+    off = torch.from_numpy(d.offsets).cuda()
+    if fused:
+        c = fp8bs.grouped_gemm_bf16_act(wl.bits_to_torch(d.a_bits).cuda(), off, qw, sw, torch.float32)
+    else:
+        qa, sa = gpu_quant_act(d.a_bits)
+        c = fp8bs.grouped_gemm(qa, sa, off, qw, sw, torch.float32)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    q_o, s_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K), s_o.reshape(E, N // 128, K // 128))
+    check_gemm(c, C_or, B, False)
