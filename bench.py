@@ -58,8 +58,8 @@ NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix, workload, bytes per launch)
     "fp8_gemm_kernel": ("fp8bs_gemm.cu", "fc78c1472f279d5c", "gemm 4096x4096x7168",
                         59.899648e6 + 13.114624e6),
-    "quantize_act_kernel": ("fp8bs_quant.cu", "fe72e534117e0c19", "act-quant 16384x7168",
-                            235.054848e6 + 83.611904e6),
+    "quantize_act_kernel": ("fp8bs_quant.cu", "27ae307a57c9158b", "act-quant 16384x7168",
+                            235.069696e6 + 83.821056e6),
     "norm_quant_kernel": ("fp8bs_norm.cu", "e3a0dae12a81a1e7", "norm-quant 16384x7168",
                           237.303808e6 + 66.459392e6),
 }
