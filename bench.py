@@ -155,6 +155,24 @@ class ClockSampler:
                 "source": "nvidia-smi -lms 50 over warm-up + timed region"}
 
 
+def max_over_ranks(elapsed_ms: float, world: int, device) -> float:
+    """The slowest rank's time (every rank gets it), then a barrier; the
+    value itself with one rank. Replicas share no data, so this max and the
+    timing barriers are the only collectives."""
+    if world <= 1:
+        return elapsed_ms
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """All ranks' work over the slowest rank's time (weak scaling: each rank
+    runs the same step on its own GPU)."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def _events(n):
     return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(n)]
@@ -218,12 +236,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
             t1.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        torch.distributed.barrier()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
 
     per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in evs])
@@ -236,7 +249,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
     del sets
     return {
         "elapsed_ms": elapsed_ms,
-        "value": world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12,
+        "value": whole_job_tflops(flops, args.steps, world, elapsed_ms),
         "n_sets": n_sets, "set_bytes": n_sets * step_in_bytes,
         "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel<dense>",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
