@@ -43,6 +43,15 @@
 //               it converts and stores its row segment.
 // The TMEM slots let the tensor cores compute the next chunks while the
 // promotion warps drain earlier ones.
+//
+// Fused-activation variant (kFused, 128 x 256 tiles, 512 threads): A arrives
+// as bf16. Warp 0 also TMA-loads each chunk's A as two 64-wide halves into a
+// 3-slot bf16 ring; warps 12-15 (converters) quantize each row's 1x128 group
+// with the activation quantizer's codec, write the E4M3 row into the stage's
+// A tile in the MMA's swizzled layout (then a proxy fence and one arrival per
+// warp on the stage barrier) and put the row's scale into an 8-deep ring that
+// the promotion warps read instead of global memory. The result is
+// bit-identical to quantizing A first and running the 128 x 256 kernel.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
