@@ -140,26 +140,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
     return true;
 }
 
-// ------------------------------------------------------------------ cp.async
-
-// 4-byte asynchronous global -> shared copy (L1-allocating).
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// Arrive once on `bar` when all earlier cp.async of this thread have landed;
-// the arrival is one of the barrier's expected arrivals (.noinc).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
@@ -489,19 +469,6 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
-}
-
-// (a0, a1) = fma((p0, p1), s2, (a0, a1)) with the accumulators held as two
-// scalars and the partial sums as raw binary32 bits.
-__device__ __forceinline__ void ffma2f(float& a0, float& a1, uint32_t p0, uint32_t p1, uint64_t s2)
-{
-    asm("{\n\t.reg .b64 t, a;\n\t"
-        "mov.b64 t, {%2, %3};\n\t"
-        "mov.b64 a, {%0, %1};\n\t"
-        "fma.rn.f32x2 a, t, %4, a;\n\t"
-        "mov.b64 {%0, %1}, a;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "r"(p0), "r"(p1), "l"(s2));
 }
 
 // ------------------------------------------------------------- packed bf16
