@@ -7,6 +7,7 @@ and weight quantization (128x128 blocks) in one launch, then the block-scaled
 GEMM with bf16 output. The headline value is GEMM FLOPs over the whole step's time
 (TFLOP/s). The same run also measures, as extra keys:
 
+* the small reference case (M=128, N=256, K=512) in microseconds,
 * the activation quantizer alone on [16384, 7168] with 0.5% outlier channels
   (GB/s against the HBM roofline),
 * RMSNorm fused with the 1x128 cast on the same [16384, 7168] shape,
@@ -17,7 +18,7 @@ GEMM with bf16 output. The headline value is GEMM FLOPs over the whole step's ti
 * the CPU oracle on a bounded sample (`cpu_baseline`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--part all|step|act_quant|norm_quant|fused|gemm2|moe] [--skip-cpu]
+                  [--part all|step|small|act_quant|norm_quant|fused|gemm2|moe] [--skip-cpu]
 
 With --gpus N > 1 (launched by torchrun) every rank runs the same step on its
 own GPU with no collective on the data path (independent replicas, weak
@@ -407,6 +408,38 @@ def bench_norm_quant(fp8bs, dev, stream, peaks, args):
             "timing": f"median of {n} launches"}
 
 
+def bench_small(fp8bs, dev, stream, args):
+    """The small reference case (M=128, N=256, K=512, FP32 out): quantize A and
+    W (one launch) + GEMM per step. A handful of CTAs: launch latency bound,
+    so it is reported in microseconds only."""
+    d = wl.cfg0(0)
+    a = wl.bits_to_torch(d.a_bits).to(dev)
+    w = wl.bits_to_torch(d.w_bits).to(dev)
+    qa = torch.empty((128, 512), dtype=torch.uint8, device=dev)
+    sa = torch.empty((128, 4), dtype=torch.float32, device=dev)
+    qw = torch.empty((256, 512), dtype=torch.uint8, device=dev)
+    sw = torch.empty((2, 4), dtype=torch.float32, device=dev)
+    c = torch.empty((128, 256), dtype=torch.float32, device=dev)
+
+    def step():
+        fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, stream)
+        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    n = max(20, min(args.steps, 200))
+    evs = _events(n)
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    stream.synchronize()
+    return {"workload": "quantize + GEMM M=128, N=256, K=512, fp32 out (reference case)",
+            "us_per_step": round(_median_ms(evs) * 1e3, 2), "launches_per_step": 2,
+            "timing": f"median of {n} steps (CUDA events); launch-latency bound"}
+
+
 def bench_gemm2(fp8bs, dev, stream, peaks, args):
     """GEMM M=4096, N=7168, K=2048 (0.5% outlier channels x50), pre-quantized
     operands, bf16 out; operands of 3 seeded sets rotated."""
@@ -578,7 +611,7 @@ def run_ours(args, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
-    parts = {"all": ("step", "act_quant", "norm_quant", "fused", "gemm2", "moe", "e2e")}.get(
+    parts = {"all": ("step", "small", "act_quant", "norm_quant", "fused", "gemm2", "moe", "e2e")}.get(
         args.part, (args.part,))
 
     result = {}
@@ -601,6 +634,8 @@ def run_ours(args, world):
             "clocks": s["clocks"],
         }
         torch.cuda.empty_cache()
+    if "small" in parts:
+        result["small_reference_case"] = bench_small(fp8bs, dev, stream, args)
     if "act_quant" in parts:
         result["act_quant"] = bench_act_quant(fp8bs, dev, stream, peaks, args)
         torch.cuda.empty_cache()
@@ -711,8 +746,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--part", choices=["all", "step", "act_quant", "norm_quant", "fused", "gemm2", "moe",
-                                       "e2e"],
+    ap.add_argument("--part", choices=["all", "step", "small", "act_quant", "norm_quant", "fused", "gemm2",
+                                       "moe", "e2e"],
                     default="all", help="which measurements to run (profiling uses one)")
     ap.add_argument("--skip-cpu", action="store_true", help="no oracle CPU baseline")
     args = ap.parse_args()
