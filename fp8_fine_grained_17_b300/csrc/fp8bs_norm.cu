@@ -240,20 +240,23 @@ norm_quant_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16_t* _
 constexpr int kWarpRowsPerCta = 8;
 constexpr int kWarpBatch = 4;
 
-template <int kB>
+template <int kB, bool kFull>
 __device__ __forceinline__ void load_batch(uint4 (&v)[kB], const uint4* src, int i0, int lane, int n_chunks,
                                            bool last_use)
 {
 #pragma unroll
     for (int b = 0; b < kB; ++b) {
         const int c = (i0 + b) * 32 + lane;
-        if (c < n_chunks)
+        if (kFull || c < n_chunks)
             v[b] = last_use ? __ldcs(src + c) : __ldg(src + c);
         else
             v[b] = make_uint4(0, 0, 0, 0);
     }
 }
 
+// kIters > 0: rows of exactly kIters batches (K = 1024 kIters), known at
+// compile time: no partial batch, no per-chunk bounds test, fixed trip counts.
+template <int kIters>
 __global__ void __launch_bounds__(32 * kWarpRowsPerCta)
 norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16_t* __restrict__ gamma,
                        const uint16_t* __restrict__ beta, int layer, float eps, int64_t M, int K,
@@ -261,11 +264,12 @@ norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16
                        float* __restrict__ mean_out, float* __restrict__ rstd_out)
 {
     constexpr int kB = kWarpBatch;
+    constexpr bool kFull = kIters > 0;
     extern __shared__ __align__(16) float4 wsm[];   // [gamma lo | gamma hi | beta lo | beta hi] x n_chunks
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int n_chunks = K >> 3;
-    const int n_iter = (n_chunks + 32 * kB - 1) / (32 * kB);   // batches per pass
+    const int n_iter = kFull ? kIters : (n_chunks + 32 * kB - 1) / (32 * kB);   // batches per pass
     const int64_t G = K >> 7;
     const float k_f = static_cast<float>(K);
     const bool has_beta = beta != nullptr;
@@ -304,7 +308,7 @@ norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int it = 0; it < n_iter; ++it) {
                 uint4 v[kB];
-                load_batch<kB>(v, src, it * kB, lane, n_chunks, false);
+                load_batch<kB, kFull>(v, src, it * kB, lane, n_chunks, false);
 #pragma unroll
                 for (int b = 0; b < kB; ++b) {
                     const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
@@ -321,10 +325,10 @@ norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int it = 0; it < n_iter; ++it) {
             uint4 v[kB];
-            load_batch<kB>(v, src, it * kB, lane, n_chunks, false);
+            load_batch<kB, kFull>(v, src, it * kB, lane, n_chunks, false);
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
-                if ((it * kB + b) * 32 + lane < n_chunks) {
+                if (kFull || (it * kB + b) * 32 + lane < n_chunks) {
                     const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -357,12 +361,12 @@ norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16
         float* srow = scale + row * G;
         for (int it = 0; it < n_iter; ++it) {
             uint4 v[kB];
-            load_batch<kB>(v, src, it * kB, lane, n_chunks, true);
+            load_batch<kB, kFull>(v, src, it * kB, lane, n_chunks, true);
             uint32_t m[kB];
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
                 const int c = (it * kB + b) * 32 + lane;
-                const int cs = c < n_chunks ? c : 0;
+                const int cs = (kFull || c < n_chunks) ? c : 0;
                 const float4 glo = wsm[cs], ghi = wsm[n_chunks + cs];
                 const float gg[8] = {glo.x, glo.y, glo.z, glo.w, ghi.x, ghi.y, ghi.z, ghi.w};
                 uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
@@ -409,7 +413,7 @@ norm_quant_warp_kernel(const uint16_t* __restrict__ x, int64_t ldx, const uint16
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
                 const int c = (it * kB + b) * 32 + lane;
-                if (c < n_chunks) {
+                if (kFull || c < n_chunks) {
                     if ((lane & 15) == 0)
                         srow[c >> 4] = d[b].s;
                     __stcs(reinterpret_cast<uint2*>(qrow + 8 * static_cast<int64_t>(c)),
@@ -445,6 +449,7 @@ fp8bs_status launch_norm(const DeviceInfo& info, const uint16_t* x, int64_t ldx,
     return launch_status();
 }
 
+template <int kIters>
 fp8bs_status launch_norm_warp(const DeviceInfo& info, const uint16_t* x, int64_t ldx, const uint16_t* gamma,
                               const uint16_t* beta, int layer, float eps, int64_t M, int K, uint8_t* q,
                               int64_t ldq, float* scale, float* mean, float* rstd, cudaStream_t stream)
@@ -461,7 +466,7 @@ fp8bs_status launch_norm_warp(const DeviceInfo& info, const uint16_t* x, int64_t
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!configured[info.device]) {
-            if (cudaFuncSetAttribute(norm_quant_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(norm_quant_warp_kernel<kIters>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kMaxSmem) != cudaSuccess) {
                 cudaGetLastError();
                 return FP8BS_ERR_CUDA;
@@ -470,7 +475,7 @@ fp8bs_status launch_norm_warp(const DeviceInfo& info, const uint16_t* x, int64_t
         }
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_quant_warp_kernel, kThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_quant_warp_kernel<kIters>, kThreads, smem) !=
             cudaSuccess ||
         per_sm <= 0) {
         cudaGetLastError();
@@ -479,8 +484,8 @@ fp8bs_status launch_norm_warp(const DeviceInfo& info, const uint16_t* x, int64_t
     const int64_t needed = (M + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
     const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
     const int grid = static_cast<int>(needed < full ? needed : full);
-    norm_quant_warp_kernel<<<grid, kThreads, smem, stream>>>(x, ldx, gamma, beta, layer, eps, M, K, q, ldq,
-                                                             scale, mean, rstd);
+    norm_quant_warp_kernel<kIters><<<grid, kThreads, smem, stream>>>(x, ldx, gamma, beta, layer, eps, M, K, q,
+                                                                     ldq, scale, mean, rstd);
     return launch_status();
 }
 
@@ -533,8 +538,19 @@ extern "C" fp8bs_status fp8bs_norm_quantize_act_1x128(const void* x, int64_t M, 
 #define FP8BS_NORM_LAUNCH(W, J) \
     launch_norm<W, J>(info, xb, ldx, gb, bb, layer, eps, M, k, q, ldq, scale, mean, rstd, s)
     // Chunks per thread: K / 8 / threads, rounded up to an instantiated count.
+    // Common hidden sizes get a kernel with the row length built in.
+#define FP8BS_NORM_WARP(I) launch_norm_warp<I>(info, xb, ldx, gb, bb, layer, eps, M, k, q, ldq, scale, mean, rstd, s)
+    switch (K) {
+    case 1024: return FP8BS_NORM_WARP(1);
+    case 2048: return FP8BS_NORM_WARP(2);
+    case 4096: return FP8BS_NORM_WARP(4);
+    case 7168: return FP8BS_NORM_WARP(7);
+    case 8192: return FP8BS_NORM_WARP(8);
+    default: break;
+    }
     if (K <= 16384)
-        return launch_norm_warp(info, xb, ldx, gb, bb, layer, eps, M, k, q, ldq, scale, mean, rstd, s);
+        return FP8BS_NORM_WARP(0);
+#undef FP8BS_NORM_WARP
     if (K <= 32768)
         return FP8BS_NORM_LAUNCH(8, 16);
     return FP8BS_NORM_LAUNCH(8, 32);
