@@ -368,33 +368,41 @@ def bench_act_quant(fp8bs, dev, stream, peaks, args):
 
 def bench_norm_quant(fp8bs, dev, stream, peaks, args):
     """RMSNorm fused with the 1x128 cast on [16384, 7168] (0.5% outlier
-    channels x100), alternating between two seeded inputs (470 MB > L2)."""
-    ns = [wl.norm(16384, 7168, seed=s) for s in (0, 1)]
+    channels x100), alternating between two seeded inputs (470 MB > L2).
+    LayerNorm with beta on the same inputs is timed beside it (it also writes
+    the row means and reads beta)."""
+    ns = [wl.norm(16384, 7168, seed=s, with_beta=True) for s in (0, 1)]
     xs = [wl.bits_to_torch(n.x_bits).to(dev) for n in ns]
     g = wl.bits_to_torch(ns[0].gamma_bits).to(dev)
+    b = wl.bits_to_torch(ns[0].beta_bits).to(dev)
     M, K = xs[0].shape
     q = torch.empty((M, K), dtype=torch.uint8, device=dev)
     s = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    mean = torch.empty(M, dtype=torch.float32, device=dev)
     rstd = torch.empty(M, dtype=torch.float32, device=dev)
-
-    def call(i):
-        fp8bs.fp8bs_norm_quantize_act_1x128(xs[i % 2], g, None, fp8bs.NORM_RMS, 1e-6, q, s,
-                                            None, rstd, stream)
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            call(i)
     n = max(20, min(args.steps, 200))
-    evs = _events(n)
-    with torch.cuda.stream(stream):
-        for i, (e0, e1) in enumerate(evs):
-            e0.record(stream)
-            call(i)
-            e1.record(stream)
-    stream.synchronize()
-    ms = _median_ms(evs)
+
+    def time_kind(kind, beta, mean_out):
+        def call(i):
+            fp8bs.fp8bs_norm_quantize_act_1x128(xs[i % 2], g, beta, kind, 1e-6, q, s,
+                                                mean_out, rstd, stream)
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                call(i)
+        evs = _events(n)
+        with torch.cuda.stream(stream):
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                call(i)
+                e1.record(stream)
+        stream.synchronize()
+        return _median_ms(evs)
+    ms = time_kind(fp8bs.NORM_RMS, None, None)
+    ms_ln = time_kind(fp8bs.NORM_LAYER, b, mean)
     groups = M * (K // 128)
     nbytes = groups * (256 + 128 + 4) + M * 4 + K * 2
     gbs = nbytes / (ms * 1e-3) / 1e9
+    nbytes_ln = nbytes + M * 4 + K * 2
     return {"workload": "RMSNorm + act-quant [16384,7168] bf16, 36 outlier channels x100",
             "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "bytes": nbytes,
             "roofline": {"bound": "hbm", "kernel": "norm_quant_kernel",
@@ -404,8 +412,11 @@ def bench_norm_quant(fp8bs, dev, stream, peaks, args):
                          "algorithmic": f"{groups} groups x 388 B (256 B read, 128 B codes, "
                                         f"4 B scale) + 4 B rstd per row + gamma",
                          "peak_note": f"of {peaks['source']} copy bandwidth"},
+            "layer_norm_beta": {"us": round(ms_ln * 1e3, 2),
+                                "GB/s": round(nbytes_ln / (ms_ln * 1e-3) / 1e9, 1),
+                                "frac": round(nbytes_ln / (ms_ln * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
             "l2": "two 235 MB inputs alternated (> 126 MB L2)",
-            "timing": f"median of {n} launches"}
+            "timing": f"median of {n} launches each"}
 
 
 def bench_small(fp8bs, dev, stream, args):

@@ -127,3 +127,15 @@ def test_norm_quant_full_size_sampled(kind):
     rows = np.sort(np.random.default_rng(1).choice(16384, 256, replace=False))
     rows = np.concatenate([[0, 1, 16382, 16383], rows])
     check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd, rows=rows)
+
+
+@pytest.mark.parametrize("kind", [orc.NORM_RMS, orc.NORM_LAYER])
+@pytest.mark.parametrize("K", [7168, 8192])
+def test_norm_quant_beta_long_rows(kind, K):
+    # Rows of 7168 / 8192 with beta run a separate instantiation; 3700 rows
+    # are more than one pass of the grid, so warps take several rows each.
+    n = wl.norm(3700, K, seed=K + kind, with_beta=True)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6)
+    rows = np.sort(np.random.default_rng(K).choice(3700, 96, replace=False))
+    rows = np.concatenate([[0, 1, 3551, 3552, 3698, 3699], rows])
+    check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd, rows=rows)
