@@ -25,6 +25,7 @@
 // loop over rows. Thread t of the CTA holds the 16-byte chunks
 // c = j * threads + t, so each warp covers 512 contiguous bytes per j and a
 // 1x128 group (16 chunks) lies in one half-warp.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -458,19 +459,19 @@ fp8bs_status launch_norm(const DeviceInfo& info, const uint16_t* x, int64_t ldx,
                          int64_t ldq, float* scale, float* mean, float* rstd, cudaStream_t stream)
 {
     constexpr int kThreads = 32 * kWarps;
-    static int per_sm[64] = {};
+    static std::atomic<int> per_sm[64] = {};   // filled once per device; racing fills store the same value
     if (info.device < 0 || info.device >= 64)
         return FP8BS_ERR_CUDA;
-    if (per_sm[info.device] == 0) {
-        int b = 0;
+    int b = per_sm[info.device].load(std::memory_order_relaxed);
+    if (b == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, norm_quant_kernel<kWarps, kJ>, kThreads, 0) !=
                 cudaSuccess || b <= 0) {
             cudaGetLastError();
             b = 1;
         }
-        per_sm[info.device] = b;
+        per_sm[info.device].store(b, std::memory_order_relaxed);
     }
-    const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[info.device];
+    const int64_t full = static_cast<int64_t>(info.sm_count) * b;
     const int grid = static_cast<int>(M < full ? M : full);
     norm_quant_kernel<kWarps, kJ><<<grid, kThreads, 0, stream>>>(x, ldx, gamma, beta, layer, eps, M, K, q,
                                                                  ldq, scale, mean, rstd);

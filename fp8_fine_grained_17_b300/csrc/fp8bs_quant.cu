@@ -6,6 +6,7 @@
 // amax-to-FP8-maximum scaling and online quantization follow the Q&A post on
 // xn--9g3bo1gtkw0l8ubf92bgle.kr, mixed-precision paragraph. The per-group
 // codec (scale, reciprocal, codes) is in fp8bs_e4m3.cuh.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -318,19 +319,21 @@ quantize_pair_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __res
 }
 
 // Resident CTAs of a kernel on the device (cached per kernel; at least 1).
+// Callers on several host threads may race to fill the cache; they all store
+// the same value.
 template <typename Kernel>
-int resident_blocks(Kernel kernel, int threads, size_t smem, int* cache)
+int resident_blocks(Kernel kernel, int threads, size_t smem, std::atomic<int>* cache)
 {
-    if (*cache == 0) {
-        int b = 0;
+    int b = cache->load(std::memory_order_relaxed);
+    if (b == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess ||
             b <= 0) {
             cudaGetLastError();
             b = 1;
         }
-        *cache = b;
+        cache->store(b, std::memory_order_relaxed);
     }
-    return *cache;
+    return b;
 }
 
 }  // namespace
@@ -365,7 +368,8 @@ static fp8bs_status quantize_act_impl(const void* x, int64_t M, int64_t K, int64
     if (ldx == K && ldq == K && total >= kTmaMinGroups) {
         static std::mutex mu;
         static bool configured[64] = {};
-        static int per_sm = 0;
+        static std::atomic<int> per_sm{0};
+        int resident = 0;
         {
             std::lock_guard<std::mutex> lock(mu);
             if (info.device < 0 || info.device >= 64)
@@ -379,28 +383,28 @@ static fp8bs_status quantize_act_impl(const void* x, int64_t M, int64_t K, int64
                 }
                 configured[info.device] = true;
             }
-            resident_blocks(quantize_act_contig_kernel, kTmaThreads, kActSmemBytes, &per_sm);
+            resident = resident_blocks(quantize_act_contig_kernel, kTmaThreads, kActSmemBytes, &per_sm);
         }
         unsigned int* err = device_error_word();
         if (err == nullptr)
             return FP8BS_ERR_CUDA;
         const int64_t chunks = (total + kTmaChunkGroups - 1) / kTmaChunkGroups;
-        const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm;
+        const int64_t full = static_cast<int64_t>(info.sm_count) * resident;
         const int grid = static_cast<int>(chunks < full ? chunks : full);
         quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err, pow2);
     } else {
         const bool contiguous = ldx == K && ldq == K;
-        static int per_sm[2] = {0, 0};
+        static std::atomic<int> per_sm[2] = {0, 0};
         const int64_t per_block = (kActThreads / 32) * 32;
         const int64_t needed = (total + per_block - 1) / per_block;
         if (contiguous) {
-            resident_blocks(quantize_act_regs_kernel<true>, kActThreads, 0, &per_sm[1]);
-            const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[1];
+            const int64_t full = static_cast<int64_t>(info.sm_count) *
+                                 resident_blocks(quantize_act_regs_kernel<true>, kActThreads, 0, &per_sm[1]);
             quantize_act_regs_kernel<true><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
                                              s>>>(xb, ldx, q, ldq, scale, G, total, pow2);
         } else {
-            resident_blocks(quantize_act_regs_kernel<false>, kActThreads, 0, &per_sm[0]);
-            const int64_t full = static_cast<int64_t>(info.sm_count) * per_sm[0];
+            const int64_t full = static_cast<int64_t>(info.sm_count) *
+                                 resident_blocks(quantize_act_regs_kernel<false>, kActThreads, 0, &per_sm[0]);
             quantize_act_regs_kernel<false><<<static_cast<int>(needed < full ? needed : full), kActThreads, 0,
                                               s>>>(xb, ldx, q, ldq, scale, G, total, pow2);
         }
