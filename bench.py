@@ -10,9 +10,11 @@ GEMM with bf16 output. The headline value is GEMM FLOPs over the whole step's ti
 * the small reference case (M=128, N=256, K=512) in microseconds,
 * the activation quantizer alone on [16384, 7168] with 0.5% outlier channels
   (GB/s against the HBM roofline),
-* RMSNorm fused with the 1x128 cast on the same [16384, 7168] shape,
+* RMSNorm (and LayerNorm with beta) fused with the 1x128 cast on the same
+  [16384, 7168] shape,
 * the headline step with the activation quantization inside the GEMM kernel,
-* the GEMM M=4096, N=7168, K=2048 with 0.5% outlier channels x50,
+* the GEMM M=4096, N=7168, K=2048 with 0.5% outlier channels x50, alone and
+  after the quantization of its operands,
 * the MoE grouped GEMM (32 experts, N=4096, K=7168, seeded top-8 routing),
 * the end-to-end step from pinned host buffers (`e2e`),
 * the CPU oracle on a bounded sample (`cpu_baseline`).
@@ -453,29 +455,47 @@ def bench_small(fp8bs, dev, stream, args):
 
 def bench_gemm2(fp8bs, dev, stream, peaks, args):
     """GEMM M=4096, N=7168, K=2048 (0.5% outlier channels x50), pre-quantized
-    operands, bf16 out; operands of 3 seeded sets rotated."""
-    qs = []
+    operands, bf16 out; operands of 3 seeded sets rotated. Timed beside it:
+    the same GEMM preceded by the quantization of both bf16 operands (one
+    launch), as a step does."""
+    qs, raw = [], []
     for seed in range(3):
         d = wl.cfg2(seed)
-        qa, sa = fp8bs.quantize_act(wl.bits_to_torch(d.a_bits).to(dev), stream)
-        qw, sw = fp8bs.quantize_weight(wl.bits_to_torch(d.w_bits).to(dev), stream)
+        a = wl.bits_to_torch(d.a_bits).to(dev)
+        w = wl.bits_to_torch(d.w_bits).to(dev)
+        qa, sa = fp8bs.quantize_act(a, stream)
+        qw, sw = fp8bs.quantize_weight(w, stream)
         qs.append((qa, sa, qw, sw))
+        raw.append((a, w))
     M, K = qs[0][0].shape
     N = qs[0][2].shape[0]
     c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
     n = max(20, min(args.steps, 200))
-    evs = _events(n)
-    with torch.cuda.stream(stream):
-        for i, (e0, e1) in enumerate(evs):
-            e0.record(stream)
-            fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
-            e1.record(stream)
-    stream.synchronize()
-    assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
-    ms = _median_ms(evs)
+
+    def timed(body):
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                body(i)
+        evs = _events(n)
+        with torch.cuda.stream(stream):
+            for i, (e0, e1) in enumerate(evs):
+                e0.record(stream)
+                body(i)
+                e1.record(stream)
+        stream.synchronize()
+        assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
+        return _median_ms(evs)
+
+    def gemm(i):
+        fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
+
+    def quantize_and_gemm(i):
+        qa, sa, qw, sw = qs[i % 3]
+        a, w = raw[i % 3]
+        fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, stream)
+        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+    ms = timed(gemm)
+    ms_step = timed(quantize_and_gemm)
     flops = 2.0 * M * N * K
     tf = flops / (ms * 1e-3) / 1e12
     fp8_peak = _fp8_peak(peaks)
@@ -484,7 +504,10 @@ def bench_gemm2(fp8bs, dev, stream, peaks, args):
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1),
                          "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
                          "frac_of_nominal_4500": round(tf / 4500.0, 4)},
-            "timing": f"median of {n} launches, 3 operand sets rotated"}
+            "with_quantize": {"us": round(ms_step * 1e3, 2),
+                              "TFLOP/s": round(flops / (ms_step * 1e-3) / 1e12, 1),
+                              "launches": 2},
+            "timing": f"median of {n} launches (or launch pairs), 3 operand sets rotated"}
 
 
 def bench_moe(fp8bs, dev, stream, peaks, args, n_tokens=wl.N_TOKENS):
