@@ -61,10 +61,10 @@ NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix, workload, bytes per launch)
     "fp8_gemm_kernel": ("fp8bs_gemm.cu", "eea353dda641b45e", "gemm 4096x4096x7168",
                         59.899648e6 + 13.114624e6),
-    "quantize_act_kernel": ("fp8bs_quant.cu", "27ae307a57c9158b", "act-quant 16384x7168",
-                            235.069696e6 + 83.821056e6),
-    "norm_quant_kernel": ("fp8bs_norm.cu", "ebd96b1dade93d11", "norm-quant 16384x7168",
-                          236.923136e6 + 66.352128e6),
+    "quantize_act_kernel": ("fp8bs_quant.cu", "f5092495d2d083e1", "act-quant 16384x7168",
+                            235.082752e6 + 82.917376e6),
+    "norm_quant_kernel": ("fp8bs_norm.cu", "198dfa477b5dc22d", "norm-quant 16384x7168",
+                          237.005824e6 + 66.628352e6),
 }
 
 
