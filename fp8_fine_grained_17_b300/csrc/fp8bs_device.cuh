@@ -58,6 +58,23 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in its stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its memory writes are visible (it returns at once for a normal launch), so
+// nothing before it may touch global memory the previous kernel writes or
+// reads. launch_dependents() lets such a dependent launch be scheduled once
+// every CTA of this grid has executed it (or exited).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Makes barrier initialisation visible to the async proxy (TMA, tcgen05).
 __device__ __forceinline__ void fence_barrier_init()
 {

@@ -324,6 +324,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         tmem_alloc<kCtas>(smem_addr(&sm.tmem_base), kTmemCols);
         tmem_relinquish<kCtas>();
     }
+    // The set-up above touches no global memory, so it may overlap the end
+    // of the previous kernel in the stream (programmatic dependent launch);
+    // from here on that kernel's results (codes, scales, offsets) are visible.
+    grid_dependency_wait();
     if (warp == 3)
         build_expert_table(sm, p, lane);
     tc_fence_before();
@@ -913,22 +917,23 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
     const int units = static_cast<int>(tile_bound < max_units ? tile_bound : max_units);
     if (units <= 0)
         return FP8BS_OK;
-    if (kCtas == 1) {
-        kernel<<<units, kThreads, smem_bytes<kCtas, kBN, kFused>(), stream>>>(map_a, map_b, p);
-        return launch_status();
-    }
+    // Programmatic dependent launch: the kernel's set-up may overlap the tail
+    // of the previous kernel in the stream (it waits for that kernel's
+    // results before its first global-memory access).
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * units);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kCtas;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(kCtas * units);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes<kCtas, kBN, kFused>();
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = kCtas == 2 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;

@@ -307,6 +307,10 @@ quantize_pair_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __res
 {
     __shared__ uint32_t warp_max[kWThreads / 32];
     __shared__ Divider block_div;
+    // The GEMM that follows in a step may be scheduled as soon as every CTA
+    // of this grid is running; it waits for this grid's results itself.
+    if (threadIdx.x == 0)
+        launch_dependents();
     const int64_t b = blockIdx.x;
     if (b < act_blocks) {
         act_regs_batch<kContiguous>((b * (kActThreads / 32) + (threadIdx.x >> 5)) * 32, x, ldx, qx, ldqx, sx,
