@@ -32,7 +32,10 @@
  *    device. The library allocates and frees nothing and never synchronizes,
  *    except fp8bs_last_device_error.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *    stream) and runs asynchronously.
+ *    stream) and runs asynchronously. The GEMM calls are launched as
+ *    programmatic dependents of the previous kernel on the stream: their
+ *    set-up may overlap that kernel's end, but they read and write no global
+ *    memory before it has completed, so stream order holds as for any launch.
  *  - Arguments are validated before anything is launched; a rejected call
  *    returns FP8BS_ERR_INVALID_ARG or FP8BS_ERR_UNSUPPORTED and touches no
  *    memory. A launch failure returns FP8BS_ERR_CUDA. Errors detected on the
