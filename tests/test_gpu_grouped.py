@@ -75,11 +75,13 @@ def test_bad_offsets_reported(orc):
 
 
 @pytest.mark.slow
-def test_moe_full_workload_sampled(orc):
-    """32 experts, N=4096, K=7168, rows from the seeded top-8 router; the full
-    launch, checked on sampled outputs (rows of every expert x two 128-column
-    blocks per expert) against per-entry float64 dot products."""
-    d = wl.moe(seed=0)
+@pytest.mark.parametrize("n_tokens", [wl.N_TOKENS, 256])
+def test_moe_full_workload_sampled(orc, n_tokens):
+    """32 experts, N=4096, K=7168, rows from the seeded top-8 router over
+    8192 tokens (prefill) or 256 (a decode batch: a few rows per expert); the
+    full launch, checked on sampled outputs (up to 16 rows of every expert x
+    two 128-column blocks per expert) against per-entry float64 dot products."""
+    d = wl.moe(seed=0, counts=wl.moe_routing(0, n_tokens=n_tokens))
     E, N, K = d.w_bits.shape
     qa, sa = gpu_quant_act(d.a_bits)
     qw, sw = gpu_quant_weight(d.w_bits.reshape(E * N, K))
