@@ -742,41 +742,58 @@ def cpu_baseline(budget_s: float = 15.0):
     7168 slice of the same GEMM (all 4096 rows when that fits the budget);
     TFLOP/s counts the sample's own FLOPs."""
     from oracle import oracle as orc
-    d, rows = _oracle_sample(orc, budget_s)
-    rows = M3 if rows >= M3 // 4 else rows
-    t = time.perf_counter()
-    _oracle_step(orc, d.a_bits[:rows], d.w_bits)
-    dt = time.perf_counter() - t
+    with _all_host_cores():
+        d, rows = _oracle_sample(orc, budget_s)
+        rows = M3 if rows >= M3 // 4 else rows
+        t = time.perf_counter()
+        _oracle_step(orc, d.a_bits[:rows], d.w_bits)
+        dt = time.perf_counter() - t
+        cores = _blas_threads()
     flops = 2.0 * rows * N3 * K3
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": _blas_threads(),
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"quantize A[{rows},{K3}] + W[{N3},{K3}] (plain C, 1 thread) and float64 "
-                      f"GEMM {rows}x{N3}x{K3} (numpy BLAS, {_blas_threads()} threads) in {dt:.2f} s",
+                      f"GEMM {rows}x{N3}x{K3} (numpy BLAS, {cores} threads) in {dt:.2f} s",
             "seconds": round(dt, 2)}
 
 
-def run_reference(args):
+def _all_host_cores():
+    """BLAS on every host core for the oracle (torchrun sets OMP_NUM_THREADS=1
+    for each rank; under torchrun only rank 0 runs the oracle)."""
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(limits=os.cpu_count() or 1, user_api="blas")
+    except Exception:
+        import contextlib
+        return contextlib.nullcontext()
+
+
+def run_reference(args, world: int = 1):
     """The oracle timed on the host cores: W + K steps, each a bounded sample
-    (rows x 4096 x 7168 slice) of the headline step."""
+    (rows x 4096 x 7168 slice) of the headline step. Under torchrun rank 0
+    alone runs it."""
     from oracle import oracle as orc
     per_step = float(np.clip(150.0 / max(1, args.steps + args.warmup), 0.5, 15.0))
-    d, rows = _oracle_sample(orc, per_step)
-    for _ in range(args.warmup):
-        _oracle_step(orc, d.a_bits[:rows], d.w_bits)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        _oracle_step(orc, d.a_bits[:rows], d.w_bits)
-    dt = time.perf_counter() - t
+    with _all_host_cores():
+        d, rows = _oracle_sample(orc, per_step)
+        for _ in range(args.warmup):
+            _oracle_step(orc, d.a_bits[:rows], d.w_bits)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            _oracle_step(orc, d.a_bits[:rows], d.w_bits)
+        dt = time.perf_counter() - t
+        cores = _blas_threads()
     flops = 2.0 * rows * N3 * K3
     value = flops * args.steps / dt / 1e12
-    cores = _blas_threads()
     sample = (f"per step: quantize A[{rows},{K3}] + W[{N3},{K3}] (plain C, 1 thread) + float64 "
               f"GEMM {rows}x{N3}x{K3} (numpy BLAS, {cores} threads)")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "sample_rows": rows},
+            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "sample_rows": rows,
+                       "ranks": "rank 0 runs the oracle on the host; other ranks exit"
+                                if world > 1 else "one process on the host"},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -801,7 +818,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_reference(args, world)), flush=True)
         return
 
     if world > 1:
