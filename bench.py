@@ -571,7 +571,7 @@ def bench_moe(fp8bs, dev, stream, peaks, args, n_tokens=wl.N_TOKENS):
             "timing": f"median of {n} launches; weights 940 MB > L2"}
 
 
-def bench_e2e(fp8bs, dev, stream, args):
+def bench_e2e(fp8bs, dev, stream, args, world=1):
     """Same step through the C entry points from pinned host buffers: every
     step copies A and W (bf16) host -> device, quantizes both (one launch),
     runs the GEMM and copies C device -> host. Uploads run on their own
@@ -625,6 +625,8 @@ def bench_e2e(fp8bs, dev, stream, args):
         step(i)
     drain()
     stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     n = max(10, min(args.steps, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -635,10 +637,10 @@ def bench_e2e(fp8bs, dev, stream, args):
     drain()
     e1.record(stream)
     stream.synchronize()
-    ms = e0.elapsed_time(e1) / n
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / n
     flops = 2.0 * M3 * N3 * K3
-    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
-            "h2d_bytes_per_step": 2 * (M3 * K3 + N3 * K3), "d2h_bytes_per_step": 2 * M3 * N3,
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": world * 2 * (M3 * K3 + N3 * K3), "d2h_bytes_per_step": world * 2 * M3 * N3,
             "ms_per_step": round(ms, 4), "steps": n,
             "path": "pinned host A, W -> H2D (upload stream, alternating buffers) -> quantize A + W "
                     "(one launch), GEMM -> D2H C (third stream); uploads and copy-back overlap "
@@ -652,8 +654,8 @@ def run_ours(args, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
-    parts = {"all": ("step", "small", "act_quant", "norm_quant", "fused", "gemm2", "moe", "e2e")}.get(
-        args.part, (args.part,))
+    parts = {"all": ("step", "small", "act_quant", "norm_quant", "fused", "gemm2", "moe", "e2e"),
+             "replicas": ("step", "e2e")}.get(args.part, (args.part,))
 
     result = {}
     if "step" in parts:
@@ -697,7 +699,7 @@ def run_ours(args, world):
         result["moe_decode"] = bench_moe(fp8bs, dev, stream, peaks, args, n_tokens=256)
         torch.cuda.empty_cache()
     if "e2e" in parts:
-        result["e2e"] = bench_e2e(fp8bs, dev, stream, args)
+        result["e2e"] = bench_e2e(fp8bs, dev, stream, args, world)
     return result
 
 
@@ -824,8 +826,8 @@ def main():
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-        if args.part != "step":
-            args.part = "step"       # extras are single-GPU measurements
+        if args.part == "all":
+            args.part = "replicas"   # the step and e2e; the extras are single-GPU measurements
     res = run_ours(args, world)
     if rank == 0:
         if world == 1 and not args.skip_cpu and args.part == "all":
