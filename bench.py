@@ -100,12 +100,16 @@ def _fp8_peak(peaks):
 
 class ClockSampler:
     """Samples SM clock, power and throttle reasons with nvidia-smi while it
-    is open (one line every 50 ms)."""
+    is open (one line every 50 ms). Entering waits (up to 10 s) for the first
+    sample, so a short timed region is never missed while nvidia-smi starts;
+    callers keep the GPU busy with the same work for at least MIN_WINDOW_S
+    after the timed region so that the record holds samples under load."""
 
     FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
     NAMED = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    MIN_WINDOW_S = 1.0
 
     def __init__(self, device: torch.device, period_ms: int = 50):
         self.cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
@@ -117,24 +121,44 @@ class ClockSampler:
             pass
         self.proc = None
         self.lines = []
+        self._thread = None
+        self._first = None
+        self.t_start = time.monotonic()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.lines.append(ln.strip())
+                self._first.set()
 
     def __enter__(self):
+        import threading
+        self._first = threading.Event()
         try:
             self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            self._thread = threading.Thread(target=self._read, daemon=True)
+            self._thread.start()
+            self._first.wait(timeout=10.0)
+        self.t_start = time.monotonic()
         return self
+
+    def elapsed(self) -> float:
+        return time.monotonic() - self.t_start
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=10)
+                self.proc.wait(timeout=10)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            if self._thread is not None:
+                self._thread.join(timeout=10)
 
     def summary(self):
         mhz, max_mhz, watts, reasons = [], None, [], set()
@@ -156,7 +180,28 @@ class ClockSampler:
                 "sm_mhz_min": min(mhz) if mhz else None,
                 "power_w_max": max(watts) if watts else None,
                 "reasons": sorted(reasons), "samples": len(mhz),
-                "source": "nvidia-smi -lms 50 over warm-up + timed region"}
+                "source": f"nvidia-smi -lms 50 over warm-up, the timed region and at least "
+                          f"{self.MIN_WINDOW_S:g} s of the same step after it"}
+
+
+def keep_busy(clk: "ClockSampler", stream, step, start: int):
+    """Runs untimed copies of `step` until the sampler has been open for
+    MIN_WINDOW_S, so that its record holds samples under the timed load."""
+    i = start
+    while clk.elapsed() < clk.MIN_WINDOW_S:
+        with torch.cuda.stream(stream):
+            for _ in range(16):
+                step(i)
+                i += 1
+        stream.synchronize()
+
+
+def line_config(world: int) -> dict:
+    """The workload both arms' lines name (identical keys and values)."""
+    return {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "out": "bf16",
+            "step": "quantize A 1x128 + quantize W 128x128 + block-scaled GEMM",
+            "l2": "inputs larger than L2 (seeded sets rotated, > 126 MB), no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def max_over_ranks(elapsed_ms: float, world: int, device) -> float:
@@ -245,6 +290,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
             t1.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
+        keep_busy(clk, stream, step, args.steps)
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     assert fp8bs.fp8bs_last_device_error(stream) == fp8bs.OK
 
@@ -666,13 +712,10 @@ def run_ours(args, world):
             "ms_per_step": round(s["elapsed_ms"] / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded numpy N(0,1) activations, N(0,0.02) weights, bf16)",
-            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "out": "bf16",
-                       "step": "quantize A 1x128 + quantize W 128x128 (one launch) + block-scaled GEMM",
-                       "kernel_events": f"per-kernel CUDA events on every {EVENT_EVERY}th timed step",
+            "config": line_config(world),
+            "method": {"kernel_events": f"per-kernel CUDA events on every {EVENT_EVERY}th timed step",
                        "launch": "the GEMM is launched as a programmatic dependent of the quantizer",
-                       "l2": f"inputs rotated over {s['n_sets']} seeded sets "
-                             f"({s['set_bytes'] / 1e6:.0f} MB > 126 MB L2), no flush",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "input_sets": f"{s['n_sets']} seeded sets, {s['set_bytes'] / 1e6:.0f} MB"},
             "roofline": s["roofline"],
             "kernels": s["kernels"],
             "gpu_launches": 2 * args.steps,
@@ -793,7 +836,8 @@ def run_reference(args, world: int = 1):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "sample_rows": rows,
+            "config": line_config(world),
+            "method": {"sample_rows": rows,
                        "ranks": "rank 0 runs the oracle on the host; other ranks exit"
                                 if world > 1 else "one process on the host"},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,

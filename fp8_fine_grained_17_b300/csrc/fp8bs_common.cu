@@ -85,21 +85,34 @@ extern "C" const char* fp8bs_status_string(fp8bs_status status)
     return "unknown status";
 }
 
+namespace {
+// Clears exactly the bits that were read, so that a bit set by a kernel on
+// another stream after the read is kept for the next call.
+__global__ void clear_error_bits(unsigned int* word, unsigned int bits)
+{
+    atomicAnd(word, ~bits);
+}
+}  // namespace
+
 extern "C" fp8bs_status fp8bs_last_device_error(fp8bs_stream_t stream)
 {
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    unsigned int* word_ptr = fp8bs::device_error_word();
+    if (word_ptr == nullptr)
+        return FP8BS_ERR_CUDA;
     unsigned int word = 0;
-    if (cudaMemcpyFromSymbol(&word, fp8bs::g_device_error, sizeof word) != cudaSuccess) {
+    if (cudaMemcpy(&word, word_ptr, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
     if (word == 0)
         return FP8BS_OK;
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(fp8bs::g_device_error, &zero, sizeof zero) != cudaSuccess) {
+    clear_error_bits<<<1, 1, 0, s>>>(word_ptr, word);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }

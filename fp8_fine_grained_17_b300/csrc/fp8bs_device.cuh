@@ -123,7 +123,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 // Returns false (after flagging the error and the CTA abort flag) if the
 // wall-clock limit passes or another role of the CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err)
+                                          unsigned int* err, unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -134,7 +134,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if ((i & 63u) == 0) {
             if (*abort_flag)
                 return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(err, DEVERR_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -155,6 +155,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
         }
     }
     return true;
+}
+
+// Adds `bytes` to the transaction count the current phase of `bar` waits for
+// (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Counts `bytes` as delivered on the current phase of `bar`, as a completed
+// copy would (used to retire bytes of a copy that was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 // ----------------------------------------------------------------------- TMA
@@ -219,6 +233,20 @@ __device__ __forceinline__ void cluster_sync_all()
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 32-bit load from another CTA's shared memory (cluster address).
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// 32-bit store to another CTA's shared memory (cluster address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // 2-D tiled TMA load into this CTA's shared memory whose completion is

@@ -53,6 +53,7 @@
 // the promotion warps read instead of global memory. The result is
 // bit-identical to quantizing A first and running the 128 x 256 kernel.
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -105,8 +106,9 @@ struct __align__(1024) Smem {
     uint8_t a[C::kStages][C::kABytes];
     uint8_t b[C::kStages][C::kBBytes];
     uint8_t abf[C::kHalfStages][C::kHalfBytes];   // fused: bf16 A halves, 128-byte swizzled
-    uint64_t full[C::kStages];            // even CTA: both CTAs' TMA bytes (+ converter warps)
+    uint64_t full[C::kStages];            // even CTA: both CTAs' TMA bytes; fused: the 4 converter warps
     uint64_t empty[C::kStages];
+    uint64_t bload[kFused ? C::kStages : 1];   // fused: the stage's W copy landed
     uint64_t bfull[C::kHalfStages];       // fused: bf16 half landed
     uint64_t bempty[C::kHalfStages];      // fused: 4 converter warps done with it
     uint64_t sa_full[C::kSaRing];         // fused: 4 converter warps wrote the chunk's scales
@@ -118,6 +120,9 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     int abort;
     int num_tiles;
+    uint32_t issued;     // chunks whose copies the producer issued (or skipped)
+    uint32_t consumed;   // chunks the MMA warp consumed
+    int skipped;         // chunk left out by the test stall injection, or -1
     // Epilogue staging, one buffer per promotion warp: 32 rows x 64 bytes,
     // rows 80 bytes apart so that 16-byte writes of a quarter warp hit
     // distinct banks.
@@ -153,6 +158,8 @@ struct Params {
     const int32_t* offsets;   // grouped only (nullptr: one expert, rows 0..M)
     int E;
     unsigned int* err;
+    unsigned long long wait_ns;   // limit of every bounded wait
+    int stall_chunk;              // test fault injection: CTA 0's producer leaves out this chunk's copies (-1: none)
 };
 
 struct Tile {
@@ -295,8 +302,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_addr(&sm.full[s]), kFused ? 5 : 1);   // fused: + 4 converter warps
+            mbar_init(smem_addr(&sm.full[s]), kFused ? 4 : 1);   // fused: the 4 converter warps
             mbar_init(smem_addr(&sm.empty[s]), 1);
+            if (kFused)
+                mbar_init(smem_addr(&sm.bload[s]), 1);
         }
         if constexpr (kFused) {
             for (int h = 0; h < C::kHalfStages; ++h) {
@@ -314,6 +323,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         }
         mbar_init(smem_addr(&sm.drain), 1);
         sm.abort = 0;
+        sm.issued = 0;
+        sm.consumed = 0;
+        sm.skipped = -1;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0 && p.KB > 0) {
@@ -366,10 +378,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 const uint32_t hp1 = ((2 * chunk + 1) / C::kHalfStages) & 1u;
                 const uint32_t s = chunk % C::kStages, sp = (chunk / C::kStages) & 1u;
                 const uint32_t ring = chunk % C::kSaRing, rp = (chunk / C::kSaRing) & 1u;
-                const bool ready = mbar_wait(smem_addr(&sm.bfull[hs0]), hp0, abort_flag, p.err) &&
-                                   mbar_wait(smem_addr(&sm.bfull[hs1]), hp1, abort_flag, p.err) &&
-                                   mbar_wait(smem_addr(&sm.empty[s]), sp ^ 1u, abort_flag, p.err) &&
-                                   mbar_wait(smem_addr(&sm.sa_empty[ring]), rp ^ 1u, abort_flag, p.err);
+                const bool ready = mbar_wait(smem_addr(&sm.bfull[hs0]), hp0, abort_flag, p.err, p.wait_ns) &&
+                                   mbar_wait(smem_addr(&sm.bfull[hs1]), hp1, abort_flag, p.err, p.wait_ns) &&
+                                   mbar_wait(smem_addr(&sm.empty[s]), sp ^ 1u, abort_flag, p.err, p.wait_ns) &&
+                                   mbar_wait(smem_addr(&sm.sa_empty[ring]), rp ^ 1u, abort_flag, p.err, p.wait_ns);
                 if (!__all_sync(0xFFFFFFFFu, ready)) {
                     ok = false;
                     break;
@@ -418,49 +430,56 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         if (warp == 0) {
             // ---------------------------------------------------- TMA producer
             // The whole warp runs the loop; one elected lane issues the copies.
-            uint32_t chunk = 0;
+            uint32_t chunk = 0;       // chunks whose copies were issued (or left out)
+            uint32_t halves = 0;      // fused: bf16 halves issued (or left out)
+            int skipped = -1;
             uint32_t s = 0, ph = 0;   // stage and its phase parity
             bool ok = true;
+            const bool stall_here = p.stall_chunk >= 0 && blockIdx.x == 0;
             Segments work = work_of(p, num_tiles, unit, n_units);
             int t, k0, k1;
             while (ok && work.next(t, k0, k1)) {
                 const Tile tile = decode_tile(sm, p, t);
                 const int32_t a_row = static_cast<int32_t>(tile.m0) + static_cast<int32_t>(rank) * BM;
                 const int32_t b_row = tile.b_row0 + static_cast<int32_t>(rank) * C::kBRows;
-                for (int kb = k0; kb < k1; ++kb, ++chunk) {
+                for (int kb = k0; kb < k1; ++kb) {
+                    const bool skip = stall_here && chunk == static_cast<uint32_t>(p.stall_chunk);
                     if constexpr (kFused) {
                         // The chunk's bf16 A as two 64-wide halves (128 B
                         // rows, 128-byte swizzle) for the converter warps.
                         for (uint32_t h = 0; h < 2; ++h) {
-                            const uint32_t hc = 2 * chunk + h;
-                            const uint32_t hs = hc % C::kHalfStages;
-                            const uint32_t hph = (hc / C::kHalfStages) & 1u;
-                            const bool free_ = mbar_wait(smem_addr(&sm.bempty[hs]), hph ^ 1u, abort_flag, p.err);
+                            const uint32_t hs = halves % C::kHalfStages;
+                            const uint32_t hph = (halves / C::kHalfStages) & 1u;
+                            const bool free_ =
+                                mbar_wait(smem_addr(&sm.bempty[hs]), hph ^ 1u, abort_flag, p.err, p.wait_ns);
                             if (!__all_sync(0xFFFFFFFFu, free_)) {
                                 ok = false;
                                 break;
                             }
-                            if (elect_one()) {
+                            if (!skip && elect_one()) {
                                 const uint32_t bar = smem_addr(&sm.bfull[hs]);
                                 mbar_arrive_expect_tx(bar, C::kHalfBytes);
                                 tma_load_2d(smem_addr(sm.abf[hs]), &map_a, bar, kb * BK + 64 * h, a_row);
                             }
                             __syncwarp();
+                            ++halves;
                         }
                         if (!ok)
                             break;
                     }
-                    const bool ready = mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err);
+                    const bool ready = mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, abort_flag, p.err, p.wait_ns);
                     if (!__all_sync(0xFFFFFFFFu, ready)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = smem_addr(&sm.full[s]);
-                    if (elect_one()) {
+                    if (!skip && elect_one()) {
                         if (kFused) {
-                            // A comes from the converter warps (their 4 arrivals).
-                            mbar_arrive_expect_tx(full, C::kBBytes);
-                            tma_load_2d(smem_addr(sm.b[s]), &map_b, full, kb * BK, b_row);
+                            // A comes from the converter warps (their 4 arrivals
+                            // on full[s]); W lands on its own barrier.
+                            const uint32_t bl = smem_addr(&sm.bload[s]);
+                            mbar_arrive_expect_tx(bl, C::kBBytes);
+                            tma_load_2d(smem_addr(sm.b[s]), &map_b, bl, kb * BK, b_row);
                         } else if (kCtas == 1) {
                             mbar_arrive_expect_tx(full, C::kStageBytes);
                             tma_load_2d(smem_addr(sm.a[s]), &map_a, full, kb * BK, a_row);
@@ -475,26 +494,43 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         }
                     }
                     __syncwarp();
+                    if (skip)
+                        skipped = static_cast<int>(chunk);
+                    ++chunk;
                     if (++s == C::kStages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
+            if (lane == 0) {
+                sm.issued = chunk;
+                sm.skipped = skipped;
+            }
             if (!ok) {
                 // Let the copies already issued land before the CTA exits.
-                if (kFused || (kCtas == 2 && !leader)) {
-                    // The fused kernel's stage barriers also count converter
-                    // arrivals, and the odd CTA's copies complete on its
-                    // partner's barrier: give the copies a fixed time.
-                    const unsigned long long t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) {
-                    }
-                } else {
-                    const uint32_t first = chunk > C::kStages ? chunk - C::kStages : 0;
-                    for (uint32_t c = first; c < chunk; ++c)
-                        mbar_wait_drain(smem_addr(&sm.full[c % C::kStages]),
-                                        (c / C::kStages) & 1u, kWaitLimitNs, p.err);
+                // A stage (a bf16 half) is refilled only after its previous
+                // chunk was consumed, which needs that chunk's copies to
+                // have landed, so only the last kStages chunks (kHalfStages
+                // halves) can still be in flight. CTA pairs retire their
+                // copies at the end of the kernel, where the even CTA knows
+                // what both CTAs issued.
+                const uint32_t c0 = chunk > C::kStages ? chunk - C::kStages : 0;
+                if constexpr (kFused) {
+                    const uint32_t h0 = halves > C::kHalfStages ? halves - C::kHalfStages : 0;
+                    for (uint32_t hc = h0; hc < halves; ++hc)
+                        if (static_cast<int>(hc / 2) != skipped)
+                            mbar_wait_drain(smem_addr(&sm.bfull[hc % C::kHalfStages]),
+                                            (hc / C::kHalfStages) & 1u, p.wait_ns, p.err);
+                    for (uint32_t c = c0; c < chunk; ++c)
+                        if (static_cast<int>(c) != skipped)
+                            mbar_wait_drain(smem_addr(&sm.bload[c % C::kStages]), (c / C::kStages) & 1u,
+                                            p.wait_ns, p.err);
+                } else if (kCtas == 1) {
+                    for (uint32_t c = c0; c < chunk; ++c)
+                        if (static_cast<int>(c) != skipped)
+                            mbar_wait_drain(smem_addr(&sm.full[c % C::kStages]), (c / C::kStages) & 1u,
+                                            p.wait_ns, p.err);
                 }
             }
         } else if (warp == 1 && leader) {
@@ -504,6 +540,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // lane every time: the warp is converged and fully active).
             uint32_t s = 0, ph = 0;   // smem stage and its phase parity
             uint32_t b = 0, tph = 0;  // TMEM slot and its phase parity
+            uint32_t consumed = 0;
             bool ok = true;
             // Descriptors of stage 0; stage s / K step k add their byte offset
             // >> 4 to the start-address field (shared addresses < 256 KB).
@@ -515,12 +552,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 for (int kb = k0; kb < k1; ++kb) {
                     const uint32_t empty_bar = smem_addr(&sm.tmem_empty[b]);
                     const uint32_t full_bar = smem_addr(&sm.full[s]);
-                    // Both conditions are usually met already: test them
+                    const uint32_t bload_bar = smem_addr(&sm.bload[kFused ? s : 0]);
+                    // The conditions are usually met already: test them
                     // together, wait only if one is not.
                     bool ready = mbar_test_wait(empty_bar, tph ^ 1u) & mbar_test_wait(full_bar, ph);
+                    if (kFused)
+                        ready = ready & mbar_test_wait(bload_bar, ph);
                     if (!__all_sync(0xFFFFFFFFu, ready)) {
-                        ready = mbar_wait(empty_bar, tph ^ 1u, abort_flag, p.err) &&
-                                mbar_wait(full_bar, ph, abort_flag, p.err);
+                        ready = mbar_wait(empty_bar, tph ^ 1u, abort_flag, p.err, p.wait_ns) &&
+                                mbar_wait(full_bar, ph, abort_flag, p.err, p.wait_ns) &&
+                                (!kFused || mbar_wait(bload_bar, ph, abort_flag, p.err, p.wait_ns));
                         if (!__all_sync(0xFFFFFFFFu, ready)) {
                             ok = false;
                             break;
@@ -538,6 +579,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         mma_commit<kCtas>(smem_addr(&sm.tmem_full[b]));
                     }
                     __syncwarp();
+                    ++consumed;
                     if (++s == C::kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -548,10 +590,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     }
                 }
             }
+            if (lane == 0)
+                sm.consumed = consumed;
             // All MMAs issued by this warp complete before TMEM is released.
             if (elect_one()) {
                 mma_commit<kCtas>(smem_addr(&sm.drain));
-                mbar_wait_drain(smem_addr(&sm.drain), 0, kWaitLimitNs, p.err);
+                mbar_wait_drain(smem_addr(&sm.drain), 0, p.wait_ns, p.err);
             }
             __syncwarp();
         }
@@ -582,7 +626,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         auto promote = [&](uint32_t c, float scale, float2 (&acc)[C::kCols / 2]) -> bool {
             const uint32_t b = c % C::kSlots;
             const bool ready = mbar_wait(smem_addr(&sm.tmem_full[b]), (c / C::kSlots) & 1u,
-                                         abort_flag, p.err);
+                                         abort_flag, p.err, p.wait_ns);
             // The warp continues only if every lane saw the phases complete:
             // the TMEM loads below are warp-collective.
             if (!__all_sync(0xFFFFFFFFu, ready))
@@ -685,7 +729,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     // product is formed in the same order as sa * sw above.
                     const uint32_t ring = chunk % C::kSaRing;
                     const bool got = mbar_wait(smem_addr(&sm.sa_full[ring]), (chunk / C::kSaRing) & 1u,
-                                               abort_flag, p.err);
+                                               abort_flag, p.err, p.wait_ns);
                     if (!__all_sync(0xFFFFFFFFu, got)) {
                         ok = false;
                         break;
@@ -769,8 +813,42 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    if (kCtas == 2)
-        cluster_sync_all();   // no remote arrival or MMA operand read is left in flight
+    if constexpr (kCtas == 2) {
+        // (A) Both CTAs' roles are done: no MMA is in flight (the even CTA's
+        // MMA warp waited for its last commit) and the counts of issued and
+        // consumed chunks are in shared memory.
+        cluster_sync_all();
+        if (leader && warp == 0) {
+            // Copies of both CTAs complete on this CTA's stage barriers. After
+            // an abort, chunks past the last one consumed may have been
+            // issued by one CTA only: make the barrier expect exactly the
+            // bytes that were issued (an arrival for a chunk only the odd CTA
+            // issued; the odd CTA's bytes retired for a chunk only this CTA
+            // issued), then wait (bounded) until they have landed. In a run
+            // without abort the range is empty.
+            const uint32_t n0 = sm.issued;
+            const uint32_t n1 = ld_cluster_u32(map_to_cta(smem_addr(&sm.issued), 1));
+            const int sk0 = sm.skipped;
+            const int sk1 = static_cast<int>(ld_cluster_u32(map_to_cta(smem_addr(&sm.skipped), 1)));
+            const uint32_t hi = n0 > n1 ? n0 : n1;
+            for (uint32_t c = sm.consumed; c < hi; ++c) {
+                const bool mine = c < n0 && static_cast<int>(c) != sk0;
+                const bool theirs = c < n1 && static_cast<int>(c) != sk1;
+                const uint32_t bar = smem_addr(&sm.full[c % C::kStages]);
+                if (elect_one()) {
+                    if (!mine && theirs)
+                        mbar_arrive_expect_tx(bar, C::kStageBytes);
+                    else if (mine && !theirs)
+                        mbar_complete_tx(bar, C::kStageBytes);
+                }
+                __syncwarp();
+                if (mine || theirs)
+                    mbar_wait_drain(bar, (c / C::kStages) & 1u, p.wait_ns, p.err);
+            }
+        }
+        // (B) Every copy into either CTA's shared memory has landed.
+        cluster_sync_all();
+    }
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc<kCtas>(tmem_base, kTmemCols);
@@ -778,6 +856,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 }
 
 // ------------------------------------------------------------------ host side
+
+// Fault injection for the failure-detection tests (fp8bs_test_inject_stall):
+// read by every GEMM launch.
+std::atomic<long long> g_stall_chunk{-1};
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
 {
@@ -896,6 +979,8 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
     p.err = device_error_word();
     if (p.err == nullptr)
         return FP8BS_ERR_CUDA;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    p.stall_chunk = static_cast<int>(g_stall_chunk.load(std::memory_order_relaxed));
     p.n_tiles = (p.N + kBN - 1) / kBN;   // a last partial tile is masked
     const int64_t tile_bound = (rows / C::kTileRows + p.E) * static_cast<int64_t>(p.n_tiles);
     if (tile_bound > 0x7FFFFFFF)
@@ -1147,4 +1232,18 @@ extern "C" fp8bs_status fp8bs_grouped_gemm_bf16_act(const void* a, int64_t lda,
     const Params p = make_params(nullptr, sw, c, out_dtype, total_M, N, K, ldc, expert_offsets, E);
     return launch<1, 256, true>(a, total_M, qw, static_cast<int64_t>(E) * N, p, K,
                                 reinterpret_cast<cudaStream_t>(stream), lda);
+}
+
+extern "C" fp8bs_status fp8bs_test_inject_stall(int64_t chunk, int64_t wait_limit_ns)
+{
+    if (chunk < 0) {
+        g_stall_chunk.store(-1);
+        g_wait_ns.store(kWaitLimitNs);
+        return FP8BS_OK;
+    }
+    if (chunk > 0x7FFFFFFF || wait_limit_ns < 100000 || wait_limit_ns > 10000000000ll)
+        return FP8BS_ERR_INVALID_ARG;
+    g_wait_ns.store(static_cast<unsigned long long>(wait_limit_ns));
+    g_stall_chunk.store(chunk);
+    return FP8BS_OK;
 }

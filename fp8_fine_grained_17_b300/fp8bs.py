@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
         L.fp8bs_last_device_error.restype = st
+        L.fp8bs_test_inject_stall.argtypes = [i64, i64]
+        L.fp8bs_test_inject_stall.restype = st
         _lib = L
     return _lib
 
@@ -246,6 +248,13 @@ def fp8bs_grouped_gemm_bf16_act(a, expert_offsets, qw, sw, c, stream=None):
 def fp8bs_last_device_error(stream=None) -> int:
     """Synchronizes the stream; returns (and clears) the device error status."""
     return lib().fp8bs_last_device_error(_stream(stream))
+
+
+def fp8bs_test_inject_stall(chunk: int, wait_limit_ns: int = 0) -> None:
+    """Failure-detection tests only: later GEMM launches leave out one chunk's
+    copies in their first CTA and give up waiting after wait_limit_ns
+    (chunk < 0 restores normal operation)."""
+    _check("fp8bs_test_inject_stall", lib().fp8bs_test_inject_stall(int(chunk), int(wait_limit_ns)))
 
 
 # ------------------------------------------------------ allocating conveniences

@@ -266,6 +266,23 @@ fp8bs_status fp8bs_grouped_gemm_bf16_act(const void *a, int64_t lda,
                                          void *c, fp8bs_out_dtype out_dtype, int64_t N, int64_t K,
                                          int64_t ldc, fp8bs_stream_t stream);
 
+/*
+ * Fault injection for failure-detection tests; not for production use.
+ * Every bounded wait of the GEMM kernels gives up after a limit (1 s by
+ * default). With chunk >= 0, every later GEMM launch of this process (any of
+ * the GEMM calls above, on any device) runs with waits limited to
+ * wait_limit_ns, and the producer of its first CTA leaves out the copies of
+ * its chunk number `chunk` (0-based over the 128-wide K chunks that CTA
+ * loads), so the waits for that chunk run out: the kernel records
+ * FP8BS_ERR_TIMEOUT for fp8bs_last_device_error, lets every copy it did
+ * issue land, releases its tensor memory and returns; output tiles of that
+ * CTA are left incomplete, nothing outside C is written. chunk < 0 restores
+ * normal operation (default limit, nothing left out). 100 us <= wait_limit_ns
+ * <= 10 s, chunk < 2^31, else FP8BS_ERR_INVALID_ARG. Not synchronized with
+ * launches in flight on other threads.
+ */
+fp8bs_status fp8bs_test_inject_stall(int64_t chunk, int64_t wait_limit_ns);
+
 /* Human-readable name of a status code (static string). */
 const char *fp8bs_status_string(fp8bs_status status);
 
@@ -274,6 +291,11 @@ const char *fp8bs_status_string(fp8bs_status status);
  * word: FP8BS_ERR_TIMEOUT if a bounded device wait expired since the last
  * call, FP8BS_ERR_INVALID_ARG if a grouped GEMM saw invalid offsets,
  * FP8BS_ERR_CUDA if the synchronization itself failed, else FP8BS_OK.
+ * There is one error word per device, shared by every stream and thread:
+ * kernels on other streams that have not finished are not waited for, and
+ * an error they record later is reported by a later call. Only the bits that
+ * were read are cleared (an atomic AND on `stream`), so no error recorded
+ * between the read and the clear is lost.
  */
 fp8bs_status fp8bs_last_device_error(fp8bs_stream_t stream);
 

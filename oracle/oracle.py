@@ -34,7 +34,11 @@ What it computes, and the passage each step follows:
   output, then the activation quantizer): "How I Improved My Deepseek In In
   The Future", paragraph of hardware suggestions (fusion of layer
   normalization and FP8 cast). Row statistics in float64 rounded once to
-  binary32; the elementwise part as binary32 numpy operations.
+  binary32; the elementwise part as binary32 numpy operations. Since a float
+  sum has no single evaluation order, the oracle also enumerates, from its
+  own statistics outward, every binary32 statistic inside a given error
+  interval and the codes each gives (``norm_stat_rings``, ``norm_rows_at``);
+  it never takes statistics from the code under test.
 """
 from __future__ import annotations
 
@@ -320,18 +324,80 @@ def norm_apply(x_bits, gamma_bits, beta_bits, kind: int, mu32, rstd32) -> np.nda
     return f32_to_bf16_bits(y)
 
 
-def norm_quantize_act_1x128(x_bits, gamma_bits, beta_bits, kind: int, eps: float,
-                            mu32=None, rstd32=None):
-    """Normalize each row, round to bf16, quantize in 1x128 tiles.
+def norm_quantize_act_1x128(x_bits, gamma_bits, beta_bits, kind: int, eps: float):
+    """Normalize each row with the oracle's own statistics, round to bf16,
+    quantize in 1x128 tiles.
 
     Returns (q uint8 [M, K], s float32 [M, K/128], mu float32 [M],
-    rstd float32 [M], y uint16 [M, K]). Given mu32/rstd32 (for example a
-    kernel's own statistics, already checked against norm_stats), the
-    elementwise part and the quantizer use those, so that every rounding
-    that decides a code is taken from the same binary32 statistics."""
+    rstd float32 [M], y uint16 [M, K])."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
-    if mu32 is None or rstd32 is None:
-        mu32, rstd32 = norm_stats(x_bits, kind, eps)
+    mu32, rstd32 = norm_stats(x_bits, kind, eps)
     y = norm_apply(x_bits, gamma_bits, beta_bits, kind, mu32, rstd32)
     q, s = quantize_act_1x128(y)
-    return q, s, np.asarray(mu32, np.float32), np.asarray(rstd32, np.float32), y
+    return q, s, mu32, rstd32, y
+
+
+# ---------------------------------------------------------------------------
+# Admissible row statistics.
+#
+# A float sum has no single correct evaluation order, so a normalization
+# layer computed in binary32 may return statistics a few units in the last
+# place away from the correctly rounded ones above; every such binary32 value
+# inside a proven error interval is an acceptable statistic, and the codes it
+# leads to are acceptable codes. These helpers enumerate those values from the
+# oracle's own statistics outward (nearest first) and evaluate the row under
+# each of them with the same elementwise steps as above.
+# ---------------------------------------------------------------------------
+
+def f32_step(v32, steps):
+    """The binary32 value `steps` representable numbers above v32 (below for
+    negative steps), walking through zero; finite values only."""
+    v = np.asarray(v32, dtype=np.float32)
+    bits = v.view(np.int32).astype(np.int64)
+    key = np.where(bits >= 0, bits, -(bits & 0x7FFFFFFF))        # monotone in the value
+    key = key + np.asarray(steps, dtype=np.int64)
+    out = np.where(key >= 0, key, (-key) | 0x80000000).astype(np.uint32)
+    return out.view(np.float32)
+
+
+def norm_stat_rings(mu32: float, rstd32: float, kind: int, mu_abs: float, rstd_rel: float,
+                    max_ring: int):
+    """Candidate binary32 statistics around (mu32, rstd32), ring by ring.
+
+    Ring d holds the pairs (mu32 stepped by i, rstd32 stepped by j) with
+    max(|i|, |j|) = d that lie within |mu - mu32| <= mu_abs and
+    |rstd - rstd32| <= rstd_rel * rstd32 (mu stays 0 for RMSNorm). Yields
+    (d, mu array, rstd array) for d = 0, 1, ... while a ring has members and
+    d <= max_ring."""
+    mu32 = np.float32(mu32)
+    rstd32 = np.float32(rstd32)
+    r_lim = float(rstd_rel) * float(rstd32)
+    for d in range(max_ring + 1):
+        if d == 0:
+            ii = np.zeros(1, np.int64)
+            jj = np.zeros(1, np.int64)
+        elif kind == NORM_RMS:
+            ii = np.zeros(2, np.int64)
+            jj = np.array([-d, d], np.int64)
+        else:
+            r = np.arange(-d, d + 1, dtype=np.int64)
+            ii = np.concatenate([np.full(r.size, -d), np.full(r.size, d), r[1:-1], r[1:-1]])
+            jj = np.concatenate([r, r, np.full(r.size - 2, -d), np.full(r.size - 2, d)])
+        mu_c = f32_step(np.full(ii.size, mu32), ii) if kind == NORM_LAYER else np.zeros(ii.size, np.float32)
+        r_c = f32_step(np.full(jj.size, rstd32), jj)
+        ok = np.abs(r_c.astype(np.float64) - float(rstd32)) <= r_lim
+        if kind == NORM_LAYER:
+            ok &= np.abs(mu_c.astype(np.float64) - float(mu32)) <= float(mu_abs)
+        if not ok.any():
+            return
+        yield d, mu_c[ok], r_c[ok]
+
+
+def norm_rows_at(x_row_bits, gamma_bits, beta_bits, kind: int, mu32, rstd32):
+    """One row normalized and quantized under each candidate (mu32[i],
+    rstd32[i]): q uint8 [n, K], s float32 [n, K/128]."""
+    x_row_bits = np.ascontiguousarray(x_row_bits, dtype=np.uint16).ravel()
+    n = len(rstd32)
+    xs = np.broadcast_to(x_row_bits, (n, x_row_bits.size))
+    y = norm_apply(xs, gamma_bits, beta_bits, kind, mu32, rstd32)
+    return quantize_act_1x128(y)

@@ -49,7 +49,11 @@ def test_clock_summary_skips_malformed_lines():
 
 def test_traffic_withdrawn_when_source_or_workload_differs(monkeypatch):
     name = "fp8_gemm_kernel"
-    fname, digest, workload, nbytes = bench.NCU_TRAFFIC[name]
+    fname, _, workload, nbytes = bench.NCU_TRAFFIC[name]
+    digest = bench._src_hash(fname)
+    current = dict(bench.NCU_TRAFFIC)
+    current[name] = (fname, digest, workload, nbytes)
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", current)
     assert bench._traffic(name, workload) == nbytes          # recorded for the current source
     assert bench._traffic(name, "some other workload") is None
     assert bench._traffic("no_such_kernel", workload) is None

@@ -1,0 +1,94 @@
+"""Failure detection on the GPU without a fault.
+
+Every wait of the GEMM kernels is bounded. The test-only injection makes the
+producer of the first CTA leave out the copies of one K chunk and shortens
+the waits to 20 ms, so the waits for that chunk run out (a barrier that
+nothing completes). The kernel must report FP8BS_ERR_TIMEOUT through
+fp8bs_last_device_error, write nothing outside C, finish every other tile
+correctly, and leave the device usable: the next normal call is correct."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from fp8_fine_grained_17_b300 import fp8bs
+from fp8_fine_grained_17_b300 import workloads as wl
+from helpers import check_gemm, gpu_quant_act, gpu_quant_weight, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+M, N, K = 256, 512, 1024          # 8 K chunks; every CTA takes one tile
+STALL_CHUNK = 3
+WAIT_NS = 20_000_000
+SENTINEL = -5.0
+
+# Rows and columns of the tile the first CTA (or CTA pair) owns.
+FIRST_TILE = {
+    fp8bs.TILE_128x256: (128, 256),
+    fp8bs.TILE_128x128: (128, 128),
+    fp8bs.TILE_PAIR_256x256: (256, 256),
+    fp8bs.TILE_PAIR_256x128: (256, 128),
+    "fused": (128, 256),
+}
+
+
+def _inputs():
+    rng = np.random.default_rng(99)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    return a, w
+
+
+def _launch(tile, a_bits, qa, sa, qw, sw, c):
+    if tile == "fused":
+        fp8bs.fp8bs_gemm_bf16_act(to_dev_bf16(a_bits), qw, sw, c)
+    else:
+        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, None, tile)
+
+
+@pytest.mark.parametrize("tile", list(FIRST_TILE))
+def test_stalled_chunk_times_out_and_device_recovers(orc, tile):
+    a_bits, w_bits = _inputs()
+    qa, sa = gpu_quant_act(a_bits)
+    qw, sw = gpu_quant_weight(w_bits)
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a_bits), *orc.quantize_weight_128x128(w_bits))
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+
+    # Output inside a guarded buffer: a row above, a row below, 64 columns right.
+    buf = torch.full((M + 2, N + 64), SENTINEL, dtype=torch.float32, device="cuda")
+    c = buf[1:M + 1, :N]
+    fp8bs.fp8bs_test_inject_stall(STALL_CHUNK, WAIT_NS)
+    try:
+        t0 = time.perf_counter()
+        _launch(tile, a_bits, qa, sa, qw, sw, c)
+        status = fp8bs.fp8bs_last_device_error()
+        elapsed = time.perf_counter() - t0
+    finally:
+        fp8bs.fp8bs_test_inject_stall(-1, 0)
+    assert status == fp8bs.ERR_TIMEOUT, fp8bs.status_string(status)
+    assert elapsed < 5.0, f"the stalled launch took {elapsed:.2f} s"
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK        # cleared by the read
+
+    # Nothing outside C was written.
+    assert torch.all(buf[0] == SENTINEL) and torch.all(buf[M + 1] == SENTINEL)
+    assert torch.all(buf[:, N:] == SENTINEL)
+    # Every tile except the first CTA's is complete and correct.
+    tr, tc = FIRST_TILE[tile]
+    got = c.cpu().numpy().astype(np.float64)
+    mask = np.ones((M, N), bool)
+    mask[:tr, :tc] = False
+    tol = 2e-5 * B + 1e-6
+    assert np.all(np.abs(got - C_or)[mask] <= tol[mask])
+
+    # The device is usable: the same call without the injection is correct.
+    c2 = torch.full((M, N), SENTINEL, dtype=torch.float32, device="cuda")
+    _launch(tile, a_bits, qa, sa, qw, sw, c2)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    check_gemm(c2, C_or, B, False)
+
+
+def test_injection_arguments_checked():
+    assert fp8bs.lib().fp8bs_test_inject_stall(0, 10) == fp8bs.ERR_INVALID_ARG
+    assert fp8bs.lib().fp8bs_test_inject_stall(1 << 40, WAIT_NS) == fp8bs.ERR_INVALID_ARG
+    assert fp8bs.lib().fp8bs_test_inject_stall(-1, 0) == fp8bs.OK

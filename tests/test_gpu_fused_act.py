@@ -106,10 +106,11 @@ def test_fused_grouped(orc, counts, N, K):
     check_gemm(c, C_or, B, True)
 
 
-def test_fused_full_size_bit_identical():
-    # The benchmarked GEMM, 4096 x 4096 x 7168, bf16 out: every output equals
-    # the unfused path's (whose parity with the oracle is tested at this size
-    # on sampled outputs in test_gpu_gemm.py).
+@pytest.mark.slow
+def test_fused_full_size(orc):
+    # The benchmarked GEMM, 4096 x 4096 x 7168, bf16 out: every output
+    # element against the float64 oracle (the oracle's quantizers, then its
+    # GEMM) and bit for bit against the unfused GPU path.
     d = wl.cfg3(0)
     a = to_dev_bf16(d.a_bits)
     qw, sw = gpu_quant_weight(d.w_bits)
@@ -117,9 +118,17 @@ def test_fused_full_size_bit_identical():
     ref = _unfused(a, qw, sw, torch.bfloat16)
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     assert torch.equal(c.view(torch.int16), ref.view(torch.int16))
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    qw_o, sw_o = orc.quantize_weight_128x128(d.w_bits)
+    C_or, B = orc.gemm(qa_o, sa_o, qw_o, sw_o)
+    check_gemm(c, C_or, B, True)
 
 
-def test_fused_moe_workload_bit_identical():
+@pytest.mark.slow
+def test_fused_moe_workload(orc):
+    # The MoE workload (32 experts, N=4096, K=7168, seeded top-8 routing of
+    # 8192 tokens): every output element against the float64 oracle and bit
+    # for bit against the unfused GPU path.
     d = wl.moe(seed=0)
     E, N, K = 32, 4096, 7168
     a = to_dev_bf16(d.a_bits)
@@ -131,3 +140,8 @@ def test_fused_moe_workload_bit_identical():
     ref = fp8bs.grouped_gemm(qa, sa, off, qw, sw, torch.bfloat16, tile=fp8bs.TILE_128x256)
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     assert torch.equal(c.view(torch.int16), ref.view(torch.int16))
+    del qa, sa, qw, sw, ref
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    qw_o, sw_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, qw_o.reshape(E, N, K), sw_o.reshape(E, N // 128, K // 128))
+    check_gemm(c, C_or, B, True)

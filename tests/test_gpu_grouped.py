@@ -76,11 +76,11 @@ def test_bad_offsets_reported(orc):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("n_tokens", [wl.N_TOKENS, 256])
-def test_moe_full_workload_sampled(orc, n_tokens):
+def test_moe_full_workload(orc, n_tokens):
     """32 experts, N=4096, K=7168, rows from the seeded top-8 router over
-    8192 tokens (prefill) or 256 (a decode batch: a few rows per expert); the
-    full launch, checked on sampled outputs (up to 16 rows of every expert x
-    two 128-column blocks per expert) against per-entry float64 dot products."""
+    8192 tokens (prefill) or 256 (a decode batch: a few rows per expert).
+    Every code and scale of both quantizations against the oracle, then every
+    output element of the grouped GEMM against the float64 oracle."""
     d = wl.moe(seed=0, counts=wl.moe_routing(0, n_tokens=n_tokens))
     E, N, K = d.w_bits.shape
     qa, sa = gpu_quant_act(d.a_bits)
@@ -88,29 +88,16 @@ def test_moe_full_workload_sampled(orc, n_tokens):
     off = torch.from_numpy(d.offsets).cuda()
     c = fp8bs.grouped_gemm(qa, sa, off, qw.view(E, N, K), sw.view(E, N // 128, K // 128))
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
-    c = c.float().cpu().numpy()
-    qa_h, sa_h = qa.cpu().numpy(), sa.cpu().numpy()
-    rng = np.random.default_rng(1)
-    worst = 0.0
-    for e in range(E):
-        lo, hi = int(d.offsets[e]), int(d.offsets[e + 1])
-        if hi == lo:
-            continue
-        rows = np.unique(rng.integers(lo, hi, min(16, hi - lo)))
-        q_rows, s_rows = orc.quantize_act_1x128(d.a_bits[rows])
-        check_codes(qa[rows], sa[rows], q_rows, s_rows)
-        for nb in rng.choice(N // 128, 2, replace=False):
-            blk = d.w_bits[e, nb * 128:(nb + 1) * 128]
-            q_b, s_b = orc.quantize_weight_128x128(blk)
-            check_codes(qw[e * N + nb * 128: e * N + (nb + 1) * 128], sw[e * (N // 128) + nb:e * (N // 128) + nb + 1], q_b, s_b)
-            rr, cc = np.meshgrid(np.arange(len(rows)), np.arange(128), indexing="ij")
-            C_or, B = orc.gemm_entries(q_rows, s_rows, q_b, s_b, rr.ravel(), cc.ravel())
-            got = c[rows[rr.ravel()], nb * 128 + cc.ravel()]
-            tol = 2e-5 * B + 1e-6 + np.abs(C_or) * 2.0 ** -8
-            err = np.abs(got - C_or)
-            assert np.all(err <= tol), (e, nb, np.max(err / tol))
-            worst = max(worst, float(np.max(err / tol)))
-    print(f"moe sampled worst err/tol {worst:.3g}")
+    qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
+    check_codes(qa, sa, qa_o, sa_o)
+    del qa, sa
+    qw_o, sw_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    check_codes(qw, sw, qw_o, sw_o)
+    del qw, sw
+    C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, qw_o.reshape(E, N, K),
+                               sw_o.reshape(E, N // 128, K // 128))
+    worst = check_gemm(c, C_or, B, True)
+    print(f"moe {n_tokens} tokens ({int(d.offsets[-1])} rows): worst err/tol {worst:.3g}")
 
 
 @pytest.mark.parametrize("tile", [fp8bs.TILE_128x256, fp8bs.TILE_128x128,

@@ -1,10 +1,11 @@
 """RMSNorm / LayerNorm fused with the 1x128 cast on the GPU against the oracle.
 
-The row statistics come from parallel sums, so they are checked against the
-oracle's float64 statistics within the bound of that summation; the codes and
-scales are then compared bit for bit with the oracle run on the kernel's own
-binary32 statistics (every rounding that decides a code taken from the same
-numbers on both sides)."""
+The row statistics come from parallel binary32 sums, so they are checked
+against the oracle's correctly rounded statistics within the proven bound of
+that summation. The codes and scales of each row must then equal the oracle's
+row at some binary32 statistic inside that bound; the oracle enumerates those
+statistics from its own values outward, so nothing computed by the kernel
+enters the oracle. How many rows needed a non-central statistic is printed."""
 import numpy as np
 import pytest
 import torch
@@ -13,19 +14,9 @@ from fp8_fine_grained_17_b300 import fp8bs
 from fp8_fine_grained_17_b300 import workloads as wl
 from oracle import oracle as orc
 
-from helpers import check_codes, to_dev_bf16
+from helpers import check_norm_rows, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
-U32 = 2.0 ** -24
-
-
-def _stat_bound(K):
-    # Each binary32 square (or centred square) enters a chain of at most
-    # K/64 + 1 lane-local additions, 5 butterfly levels and up to 8 warp
-    # partials: relative error of the sum <= (K/64 + 15) u. 1/sqrt halves it;
-    # the division, +eps and the rounded 1/sqrt add 3 u, and the oracle's
-    # own rounding to binary32 one more.
-    return ((K / 64 + 15) / 2 + 4) * U32
 
 
 def run_norm(x_bits, g_bits, b_bits, kind, eps, ldx=None, ldq=None):
@@ -50,28 +41,17 @@ def run_norm(x_bits, g_bits, b_bits, kind, eps, ldx=None, ldq=None):
 
 
 def check_norm(x_bits, g_bits, b_bits, kind, eps, q, s, mean_k, rstd_k, rows=None):
-    """Compare the listed rows (all by default)."""
+    """Compare the listed rows (all by default); print the non-central count."""
     q = q.cpu().numpy() if torch.is_tensor(q) else q
     s = s.cpu().numpy() if torch.is_tensor(s) else s
     if rows is not None:
         x_bits = x_bits[rows]
         q, s = q[rows], s[rows]
         mean_k, rstd_k = mean_k[rows], rstd_k[rows]
-    K = x_bits.shape[1]
-    mu_or, r_or = orc.norm_stats(x_bits, kind, eps)
-    rel = np.abs(rstd_k.astype(np.float64) - r_or) / r_or
-    assert rel.max() <= _stat_bound(K), f"rstd off by {rel.max() / U32:.1f} u"
-    if kind == orc.NORM_LAYER:
-        mag = np.abs(orc.bf16_bits_to_f32(x_bits).astype(np.float64)).mean(axis=1)
-        err = np.abs(mean_k.astype(np.float64) - mu_or)
-        assert np.all(err <= (K / 64 + 16) * U32 * mag + U32 * np.abs(mu_or))
-        mu = mean_k
-    else:
-        mu = np.zeros_like(rstd_k)
-    q_or, s_or, _, _, _ = orc.norm_quantize_act_1x128(x_bits, g_bits, b_bits, kind, eps,
-                                                      mu32=mu, rstd32=rstd_k)
-    check_codes(torch.from_numpy(np.ascontiguousarray(q)), torch.from_numpy(np.ascontiguousarray(s)),
-                q_or, s_or)
+    n, off, ring = check_norm_rows(orc, x_bits, g_bits, b_bits, kind, eps, q, s, mean_k, rstd_k)
+    print(f"norm kind={kind} K={x_bits.shape[1]}: {n} rows, {off} matched a non-central "
+          f"statistic (farthest {ring} ulp)")
+    return off
 
 
 SHAPES = [(1, 128), (5, 384), (37, 1024), (64, 2048), (33, 4096), (19, 5120), (70, 7168),
@@ -108,14 +88,18 @@ def test_norm_quant_degenerate_rows():
 
 
 def test_norm_quant_matches_unfused_gpu_quantizer():
-    # The fused kernel's codes equal the 1x128 quantizer kernel applied to the
-    # normalized bf16 rows (here formed on the host from the kernel's own
-    # statistics), so the fusion changes nothing but the memory traffic.
+    # Where the fused kernel's rows equal the oracle's central rows (checked
+    # first), the 1x128 quantizer kernel applied to the oracle's normalized
+    # bf16 rows gives the same codes and scales: the fusion changes nothing
+    # but the memory traffic.
     n = wl.norm(96, 7168, seed=8, with_beta=False)
     q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, None, orc.NORM_RMS, 1e-6)
-    y = orc.norm_apply(n.x_bits, n.gamma_bits, None, orc.NORM_RMS, np.zeros_like(rstd), rstd)
-    q2, s2 = fp8bs.quantize_act(to_dev_bf16(y))
-    assert torch.equal(q, q2) and torch.equal(s, s2)
+    q_c, s_c, _, _, y = orc.norm_quantize_act_1x128(n.x_bits, n.gamma_bits, None, orc.NORM_RMS, 1e-6)
+    rows = np.flatnonzero(np.all(q.cpu().numpy() == q_c, axis=1) &
+                          np.all(s.cpu().numpy().view(np.uint32) == s_c.view(np.uint32), axis=1))
+    assert rows.size >= 48
+    q2, s2 = fp8bs.quantize_act(to_dev_bf16(y[rows]))
+    assert torch.equal(q[rows].cpu(), q2.cpu()) and torch.equal(s[rows].cpu(), s2.cpu())
 
 
 @pytest.mark.parametrize("kind", [orc.NORM_RMS, orc.NORM_LAYER])

@@ -152,3 +152,66 @@ def test_power_of_two_scale_invariance(kind):
         for a_, b_ in zip((ref[0], ref[1], ref[4]), (got[0], got[1], got[4])):
             assert np.array_equal(a_, b_)
         assert np.array_equal(got[3], ref[3] * np.float32(2.0 ** -j))
+
+
+def test_f32_step_walks_representable_values():
+    v = np.float32([1.0, -1.0, 0.0, 3.5e-3, -7.25e4, 2.0 ** -126])
+    up = orc.f32_step(v, 1)
+    down = orc.f32_step(v, -1)
+    assert np.array_equal(up, np.nextafter(v, np.float32(np.inf)))
+    assert np.array_equal(down, np.nextafter(v, np.float32(-np.inf)))
+    # Several steps equal repeated nextafter, across a binade and through zero.
+    w = np.float32(2.0)
+    for _ in range(5):
+        w = np.nextafter(w, np.float32(-np.inf))
+    assert orc.f32_step(np.float32(2.0), -5) == w
+    z = np.float32(0.0)
+    for _ in range(3):
+        z = np.nextafter(z, np.float32(-np.inf))
+    assert orc.f32_step(np.float32(1e-45), -4) == z
+    assert orc.f32_step(orc.f32_step(np.float32(0.3), 17), -17) == np.float32(0.3)
+
+
+def test_stat_rings_cover_the_interval_once():
+    # Every binary32 pair inside the interval appears in exactly one ring, the
+    # oracle's own pair first; nothing outside the interval appears.
+    mu, r = np.float32(0.0625), np.float32(1.5)
+    mu_abs = 5 * float(np.spacing(mu))
+    r_rel = 3 * float(np.spacing(r)) / float(r)
+    seen = []
+    rings = list(orc.norm_stat_rings(mu, r, orc.NORM_LAYER, mu_abs, r_rel, max_ring=50))
+    assert rings[0][0] == 0 and rings[0][1][0] == mu and rings[0][2][0] == r
+    for d, mus, rs in rings:
+        seen += list(zip(mus.tolist(), rs.tolist()))
+    # Brute force over a wide grid of neighbours, kept by value. 0.0625 is a
+    # power of two: below it the spacing halves, so 10 steps fit there.
+    want = set()
+    for i in range(-40, 41):
+        for j in range(-40, 41):
+            m2, r2 = orc.f32_step(mu, i), orc.f32_step(r, j)
+            if abs(float(m2) - float(mu)) <= mu_abs and abs(float(r2) - float(r)) <= r_rel * float(r):
+                want.add((float(m2), float(r2)))
+    assert len(want) == 16 * 7
+    assert len(seen) == len(set(seen)) == len(want) and set(seen) == want
+    assert rings[-1][0] == 10
+    # RMSNorm: mu stays 0, rstd walks outward symmetrically.
+    rms = list(orc.norm_stat_rings(0.0, r, orc.NORM_RMS, 0.0, r_rel, max_ring=50))
+    assert [d for d, _, _ in rms] == [0, 1, 2, 3]
+    assert all(np.all(m == 0) for _, m, _ in rms)
+
+
+def test_rows_at_equals_full_path_at_central_statistics():
+    # Evaluating a row under the oracle's own statistics through the candidate
+    # path gives the rows of norm_quantize_act_1x128; a wrong rstd changes codes.
+    for kind in (orc.NORM_RMS, orc.NORM_LAYER):
+        x, g, b = _rows(6, 896, seed=21 + kind, outliers=100.0)
+        q, s, mu, rstd, _ = orc.norm_quantize_act_1x128(x, g, b, kind, 1e-6)
+        for i in range(6):
+            qc, sc = orc.norm_rows_at(x[i], g, b, kind, mu[i:i + 1], rstd[i:i + 1])
+            assert np.array_equal(qc[0], q[i]) and np.array_equal(sc[0], s[i])
+        # A rstd about 25% larger scales y, hence every group's amax and
+        # scale (the codes, being scale-free, mostly stay).
+        far = orc.f32_step(rstd[:1], 1 << 21)
+        assert 1.2 < far[0] / rstd[0] < 1.3
+        _, sf = orc.norm_rows_at(x[0], g, b, kind, mu[:1], far)
+        assert np.all(sf[0] != s[0])
