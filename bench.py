@@ -252,6 +252,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
     qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
     sw = torch.empty((N3 // 128, K3 // 128), dtype=torch.float32, device=dev)
     c = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+    ws = fp8bs.workspace(M3, N3, K3, device=dev)   # the GEMM splits its last wave of tiles
 
     # The two quantizations are independent and run as one launch
     # (fp8bs_quantize_act_and_weight); the GEMM follows on the same stream.
@@ -262,7 +263,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
         fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, stream)
         if ev is not None:
             ev[1].record(stream)
-        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+        fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, ws, stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -306,7 +307,7 @@ def bench_step(fp8bs, dev, stream, peaks, args, world):
         "elapsed_ms": elapsed_ms,
         "value": whole_job_tflops(flops, args.steps, world, elapsed_ms),
         "n_sets": n_sets, "set_bytes": n_sets * step_in_bytes,
-        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel<dense>",
+        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel<2,256> (CTA pair, 256x256 tiles, last wave split)",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
                      "traffic": _traffic("fp8_gemm_kernel", "gemm 4096x4096x7168"),
@@ -341,6 +342,7 @@ def bench_fused(fp8bs, dev, stream, peaks, args):
     qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
     sw = torch.empty((N3 // 128, K3 // 128), dtype=torch.float32, device=dev)
     c = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+    ws = fp8bs.workspace(M3, N3, K3, device=dev)
     n = max(20, min(args.steps, 400))
 
     def run(fused):
@@ -358,7 +360,7 @@ def bench_fused(fp8bs, dev, stream, peaks, args):
                     fp8bs.fp8bs_gemm_bf16_act(a, qw, sw, c, stream)
                 else:
                     fp8bs.fp8bs_quantize_act_1x128(a, qa, sa, stream)
-                    fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+                    fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, ws, stream)
                 if ev is not None:
                     ev[2].record(stream)
         stream.synchronize()
@@ -523,6 +525,7 @@ def bench_gemm2(fp8bs, dev, stream, peaks, args):
     M, K = qs[0][0].shape
     N = qs[0][2].shape[0]
     c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = fp8bs.workspace(M, N, K, device=dev)
     n = max(20, min(args.steps, 200))
 
     def timed(body):
@@ -540,13 +543,13 @@ def bench_gemm2(fp8bs, dev, stream, peaks, args):
         return _median_ms(evs)
 
     def gemm(i):
-        fp8bs.fp8bs_gemm(*qs[i % 3], c, stream)
+        fp8bs.fp8bs_gemm_ws(*qs[i % 3], c, ws, stream)
 
     def quantize_and_gemm(i):
         qa, sa, qw, sw = qs[i % 3]
         a, w = raw[i % 3]
         fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, stream)
-        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, stream)
+        fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, ws, stream)
     ms = timed(gemm)
     ms_step = timed(quantize_and_gemm)
     flops = 2.0 * M * N * K
@@ -635,6 +638,7 @@ def bench_e2e(fp8bs, dev, stream, args, world=1):
     qw = torch.empty((N3, K3), dtype=torch.uint8, device=dev)
     sw = torch.empty((N3 // 128, K3 // 128), dtype=torch.float32, device=dev)
     c = [torch.empty((M3, N3), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ws = fp8bs.workspace(M3, N3, K3, device=dev)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     in_ready = [torch.cuda.Event(), torch.cuda.Event()]
@@ -654,7 +658,7 @@ def bench_e2e(fp8bs, dev, stream, args, world=1):
             stream.wait_event(out_done[b])     # step i-2's copy-out of C[b] is done
             fp8bs.fp8bs_quantize_act_and_weight(a[b], qa, sa, w[b], qw, sw, stream)
             consumed[b].record(stream)
-            fp8bs.fp8bs_gemm(qa, sa, qw, sw, c[b], stream)
+            fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c[b], ws, stream)
             gemm_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(gemm_done[b])

@@ -171,6 +171,44 @@ __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
     asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Global-memory flag handshake between CTAs of one grid.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag == value (each calling thread acquires it). Bounded like
+// mbar_wait: false after the limit (error recorded, abort flag raised) or
+// when another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_flag(const unsigned int* flag, uint32_t value, volatile int* abort_flag,
+                                          unsigned int* err, unsigned long long limit_ns)
+{
+    if (ld_acquire_gpu(flag) == value)
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) == value)
+            return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicOr(err, DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
@@ -187,6 +225,31 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// Contiguous bulk copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from this CTA's shared memory to global memory, in the calling
+// thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// Closes the calling thread's current bulk async-group and waits until all
+// its groups have completed (their writes performed).
+__device__ __forceinline__ void bulk_commit_and_wait()
+{
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Orders this thread's async-proxy (bulk copy) global writes before its
+// later generic-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // 2-D tiled load of box (x, y) into shared memory; completion is counted in
@@ -438,6 +501,18 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32])
                    "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
                    "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
                    "+r"(v[30]), "+r"(v[31])::"memory");
+}
+
+// Waits for this thread's outstanding tcgen05.ld; both destination arrays
+// are tied in.
+__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[16], uint32_t (&b)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+                   "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+                   "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
+                   "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
+                   "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])::"memory");
 }
 
 // Orders later uses of v after an earlier tcgen05.wait::ld that covered the

@@ -71,13 +71,19 @@ constexpr int BK = 128;   // K chunk = one scale group
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 512;
 constexpr int kEpiRowBytes = 80;
-constexpr int kProducerRegs = 56;
 
 // kFused: A arrives as bf16 and is quantized to E4M3 1x128 tiles inside the
 // kernel (four converter warps, warps 12-15) instead of being read as
 // pre-quantized codes; the rest of the pipeline is unchanged.
 template <int kCtas, int kBN, bool kFused = false>
 struct Cfg {
+    // Promotion warps: two column groups of four (TMEM lanes repeat every
+    // four warps). Measured on B300: a chunk's promotion is bound by the
+    // TMEM read bandwidth plus the packed-FMA pipe, which do not overlap;
+    // sixteen warps (four column groups) read TMEM faster in isolation but
+    // made the whole kernel 10 % slower.
+    static constexpr int kPromo = 8;
+    static constexpr int kGroups = kPromo / 4;
     static constexpr int kBRows = kBN / kCtas;            // W rows staged per CTA
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = kBRows * BK;
@@ -85,15 +91,21 @@ struct Cfg {
     // The fused kernel gives 48 KB to its bf16 ring, so it keeps 3 stages.
     static constexpr int kStages = kFused ? 3 : (192 * 1024) / kStageBytes;   // 4, 6 or 8
     static constexpr int kSlots = kTmemCols / kBN;        // TMEM accumulator slots
-    static constexpr int kCols = kBN / 2;                 // columns per promotion thread
+    static constexpr int kCols = kBN / kGroups;           // columns per promotion thread
     static constexpr int kTileRows = BM * kCtas;          // output rows per tile
     static constexpr int kTileN = kBN;                    // output columns per tile
     static constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * kCtas, kBN);
-    static constexpr int kThreads = kFused ? 512 : 384;
+    static constexpr int kCtrlThreads = kFused ? 256 : 128;   // warps 0-3 (+ the converters)
+    static constexpr int kThreads = kCtrlThreads + 32 * kPromo;
     // Registers per thread after setmaxnreg: warps 0-3 (and the converters)
     // shrink, the promotion warps grow; the sums equal the launch budget
-    // (65536 per CTA).
-    static constexpr int kEpilogueRegs = kFused ? 200 : 224;
+    // (the whole register file over the CTA's threads, in steps of 8).
+    static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
+    static constexpr int kCtrlRegs = 56;
+    static constexpr int kEpilogueRegs =
+        ((kLaunchRegs * kThreads - kCtrlRegs * kCtrlThreads) / (32 * kPromo)) & ~7;
+    static_assert(kEpilogueRegs <= 256 && kCtrlRegs * kCtrlThreads + kEpilogueRegs * 32 * kPromo <=
+                      kLaunchRegs * kThreads, "register split");
     // bf16 A ring (fused only): half chunks of 128 rows x 64 K (16 KB).
     static constexpr int kHalfStages = kFused ? 3 : 1;
     static constexpr int kHalfBytes = kFused ? BM * 64 * 2 : 16;
@@ -117,6 +129,7 @@ struct __align__(1024) Smem {
     uint64_t tmem_full[C::kSlots];
     uint64_t tmem_empty[C::kSlots];       // even CTA: 8 arrivals per CTA of the pair
     uint64_t drain;
+    uint64_t part_bar[8];  // split waves: a promotion warp's partial tile landed in shared memory
     uint32_t tmem_base;
     int abort;
     int num_tiles;
@@ -126,7 +139,7 @@ struct __align__(1024) Smem {
     // Epilogue staging, one buffer per promotion warp: 32 rows x 64 bytes,
     // rows 80 bytes apart so that 16-byte writes of a quarter warp hit
     // distinct banks.
-    alignas(16) uint8_t epi[8][32 * kEpiRowBytes];
+    alignas(16) uint8_t epi[C::kPromo][32 * kEpiRowBytes];
     int tile_start[kMaxExperts + 1];   // first tile index of each expert
     int row_start[kMaxExperts + 1];    // copy of expert_offsets
 };
@@ -160,6 +173,16 @@ struct Params {
     unsigned int* err;
     unsigned long long wait_ns;   // limit of every bounded wait
     int stall_chunk;              // test fault injection: CTA 0's producer leaves out this chunk's copies (-1: none)
+    // Split of the last, partial wave of tiles (dense launches with a
+    // workspace): the last sk_tiles tiles are each computed as sk_split
+    // ranges of K chunks by different work units. Piece j > 0 writes its
+    // FP32 partial tile to sk_part[slot] and sets its warp's flag to `epoch`;
+    // piece 0's unit adds the partials in piece order and stores C.
+    int sk_tiles;                 // 0: no split
+    int sk_split;
+    float* sk_part;               // [slot][kCtas][8 warps][kCols / 4][32 lanes] float4
+    unsigned int* sk_flag;        // [slot][kCtas][8 warps]
+    unsigned int epoch;
 };
 
 struct Tile {
@@ -201,29 +224,47 @@ __device__ __forceinline__ Tile decode_tile(const S& sm, const Params& p, int t)
     return tile;
 }
 
-// The tiles of one work unit (CTA, or CTA pair): unit, unit + n_units, ...,
-// each as the K-chunk range [k0, k1) = [0, KB).
+// The work of one unit (CTA, or CTA pair): the whole tiles unit,
+// unit + n_units, ... below full_end (K chunks [0, KB)), then, when the last
+// wave is split, piece `piece` of tile full_end + piece / split: K chunks
+// [j KB / split, (j + 1) KB / split) with j = piece % split.
 struct Segments {
-    int t, step, num_tiles, KB;
+    int t, step, full_end, KB;
+    int piece, split;
+    int cur;   // piece index (within its tile) of the range last handed out; 0 for a whole tile
     __device__ __forceinline__ bool next(int& tile, int& k0, int& k1)
     {
-        if (t >= num_tiles)
+        if (t < full_end) {
+            tile = t;
+            k0 = 0;
+            k1 = KB;
+            t += step;
+            cur = 0;
+            return true;
+        }
+        if (piece < 0)
             return false;
-        tile = t;
-        k0 = 0;
-        k1 = KB;
-        t += step;
+        cur = piece % split;
+        tile = full_end + piece / split;
+        k0 = cur * KB / split;
+        k1 = (cur + 1) * KB / split;
+        piece = -1;
         return true;
     }
 };
 
+template <bool kSplit>
 __device__ __forceinline__ Segments work_of(const Params& p, int num_tiles, int unit, int n_units)
 {
     Segments w;
     w.KB = p.KB;
-    w.num_tiles = num_tiles;
     w.t = unit;
     w.step = n_units;
+    const bool split = kSplit && p.sk_tiles > 0 && p.sk_split > 1 && num_tiles >= p.sk_tiles;
+    w.full_end = split ? num_tiles - p.sk_tiles : num_tiles;
+    w.split = split ? p.sk_split : 1;
+    w.piece = split && unit < p.sk_tiles * p.sk_split ? unit : -1;
+    w.cur = 0;
     return w;
 }
 
@@ -279,7 +320,10 @@ __device__ void build_expert_table(S& sm, const Params& p, int lane)
     }
 }
 
-template <int kCtas, int kBN, bool kFused = false>
+// kSplit: the launch splits its last wave (the instantiation that carries
+// the partial-tile hand-over; launches without a split use the other one, so
+// their promotion loop is compiled without that code).
+template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
 __global__ void __launch_bounds__(Cfg<kCtas, kBN, kFused>::kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p)
@@ -314,14 +358,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
             for (int i = 0; i < C::kSaRing; ++i) {
                 mbar_init(smem_addr(&sm.sa_full[i]), 4);
-                mbar_init(smem_addr(&sm.sa_empty[i]), 8);
+                mbar_init(smem_addr(&sm.sa_empty[i]), C::kPromo);
             }
         }
         for (int b = 0; b < C::kSlots; ++b) {
             mbar_init(smem_addr(&sm.tmem_full[b]), 1);
-            mbar_init(smem_addr(&sm.tmem_empty[b]), 8 * kCtas);   // one per promotion warp
+            mbar_init(smem_addr(&sm.tmem_empty[b]), C::kPromo * kCtas);   // one per promotion warp
         }
         mbar_init(smem_addr(&sm.drain), 1);
+        for (int w = 0; w < 8; ++w)
+            mbar_init(smem_addr(&sm.part_bar[w]), 1);
         sm.abort = 0;
         sm.issued = 0;
         sm.consumed = 0;
@@ -352,8 +398,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     const int num_tiles = sm.num_tiles;
     volatile int* abort_flag = &sm.abort;
 
-    if (kFused && warp >= 12) {
-        regs_dec<kProducerRegs>();
+    if (kFused && warp >= 4 + C::kPromo) {
+        regs_dec<C::kCtrlRegs>();
         // -------------------------------------------------- A converters
         // Warp cw handles rows 32 pass + 8 cw + lane/4 (pass = 0..3) of the
         // chunk; the lane quad t = lane & 3 of a row holds its 16-byte
@@ -364,12 +410,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         // (same codec); codes go to the stage's A tile in the MMA's
         // 128-byte-swizzled layout, scales to the ring the promotion warps
         // read.
-        const int cw = warp - 12;
+        const int cw = warp - 4 - C::kPromo;
         const int qrow = lane >> 2;
         const int t4 = lane & 3;
         uint32_t chunk = 0;
         bool ok = true;
-        Segments work = work_of(p, num_tiles, unit, n_units);
+        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
         int t, k0, k1;
         while (ok && work.next(t, k0, k1)) {
             for (int kb = k0; kb < k1; ++kb, ++chunk) {
@@ -426,7 +472,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
         }
     } else if (warp < 4) {
-        regs_dec<kProducerRegs>();
+        regs_dec<C::kCtrlRegs>();
         if (warp == 0) {
             // ---------------------------------------------------- TMA producer
             // The whole warp runs the loop; one elected lane issues the copies.
@@ -436,7 +482,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             uint32_t s = 0, ph = 0;   // stage and its phase parity
             bool ok = true;
             const bool stall_here = p.stall_chunk >= 0 && blockIdx.x == 0;
-            Segments work = work_of(p, num_tiles, unit, n_units);
+            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
             int t, k0, k1;
             while (ok && work.next(t, k0, k1)) {
                 const Tile tile = decode_tile(sm, p, t);
@@ -546,7 +592,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // >> 4 to the start-address field (shared addresses < 256 KB).
             const uint64_t adesc0 = smem_desc_k_sw128(smem_addr(sm.a[0]));
             const uint64_t bdesc0 = smem_desc_k_sw128(smem_addr(sm.b[0]));
-            Segments work = work_of(p, num_tiles, unit, n_units);
+            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
             int t, k0, k1;
             while (ok && work.next(t, k0, k1)) {
                 for (int kb = k0; kb < k1; ++kb) {
@@ -603,7 +649,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         regs_inc<C::kEpilogueRegs>();
         // ------------------------------------------------------- promotion
         const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 4) >> 2;      // output columns kCols*half .. +kCols-1
+        const int half = (warp - 4) >> 2;      // column group: output columns kCols*half .. +kCols-1
         const int r = quarter * 32 + lane;
         // The slot-free arrivals of both CTAs of a pair go to the even CTA
         // (tmem_empty[b] is at tmem_empty[0] + 8 b bytes).
@@ -654,6 +700,39 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     acc[16 + i] = __ffma2_rn(
                         make_float2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1])),
                         scale2, acc[16 + i]);
+            } else if constexpr (C::kCols == 128) {
+                // Column blocks of 16, loaded two at a time: blocks j+2 and
+                // j+3 are in flight while j and j+1 are accumulated (three
+                // buffers; one wait per pair of loads); the slot goes back
+                // once the last pair has arrived.
+                constexpr int kBlocks = 8;
+                uint32_t v[3][16];
+                tmem_ld_32x32b_x16(taddr, v[0]);
+                tmem_ld_32x32b_x16(taddr + 16, v[1]);
+                tmem_ld_wait2(v[0], v[1]);
+#pragma unroll
+                for (int j = 0; j < kBlocks; j += 2) {
+                    const bool more = j + 2 < kBlocks;
+                    if (more)
+                        tmem_ld_32x32b_x16(taddr + 16 * (j + 2), v[(j + 2) % 3]);
+                    else
+                        give_slot(c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[8 * j + i] = __ffma2_rn(make_float2(__uint_as_float(v[j % 3][2 * i]),
+                                                                __uint_as_float(v[j % 3][2 * i + 1])),
+                                                    scale2, acc[8 * j + i]);
+                    if (more)
+                        tmem_ld_32x32b_x16(taddr + 16 * (j + 3), v[j % 3]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[8 * (j + 1) + i] =
+                            __ffma2_rn(make_float2(__uint_as_float(v[(j + 1) % 3][2 * i]),
+                                                   __uint_as_float(v[(j + 1) % 3][2 * i + 1])),
+                                       scale2, acc[8 * (j + 1) + i]);
+                    if (more)
+                        tmem_ld_wait2(v[(j + 2) % 3], v[j % 3]);
+                }
             } else {
                 // Column blocks j of 16: the load of block j+1 is in flight
                 // while block j is accumulated; the slot goes back once the
@@ -679,7 +758,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
             return true;
         };
-        Segments work = work_of(p, num_tiles, unit, n_units);
+        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
         int t, k0, k1;
         while (ok && work.next(t, k0, k1)) {
             const Tile tile = decode_tile(sm, p, t);
@@ -692,38 +771,39 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 acc[i] = make_float2(0.0f, 0.0f);
             // Scales straight from global memory: a thread's activation
             // scales sa[row, :] are contiguous, and the warp's weight scales
-            // sw[e, n-block, :] are one broadcast address. They are read four
-            // chunks at a time, one batch ahead of use (latency hidden), and
-            // rotated as chunks are consumed. Rows past the end read the last
-            // row; their results are never stored.
+            // sw[e, n-block, :] are one broadcast address. Each is read two
+            // chunks ahead of its use (latency hidden; one chunk in the fused
+            // kernel). Rows past the end
+            // read the last row; their results are never stored.
             const int64_t srow = min(tile.m0 + rank * BM + r, p.rows - 1);
             const float* sa_row = kFused ? nullptr : p.sa + srow * p.KB;
             const float* sw_row =
                 p.sw + (static_cast<int64_t>(tile.expert) * p.NB + min(n_col / 128, p.NB - 1)) * p.KB;
-            auto load4 = [&](int kb0, float4& a4, float4& w4) {
-                const int last = p.KB - 1;
-                if constexpr (kFused)
-                    a4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);   // activation scales come from the ring
-                else
-                    a4 = make_float4(__ldg(sa_row + min(kb0, last)), __ldg(sa_row + min(kb0 + 1, last)),
-                                     __ldg(sa_row + min(kb0 + 2, last)), __ldg(sa_row + min(kb0 + 3, last)));
-                w4 = make_float4(__ldg(sw_row + min(kb0, last)), __ldg(sw_row + min(kb0 + 1, last)),
-                                 __ldg(sw_row + min(kb0 + 2, last)), __ldg(sw_row + min(kb0 + 3, last)));
-            };
-            float4 cs;       // sa * sw of the current batch, rotated per chunk
-            float4 na, nw;   // next batch, in flight
+            const int last = p.KB - 1;
+            // In the fused kernel the activation scales come from the ring.
+            auto ld_sa = [&](int kb) { return kFused ? 1.0f : __ldg(sa_row + min(kb, last)); };
+            auto ld_sw = [&](int kb) { return __ldg(sw_row + min(kb, last)); };
+            float a1 = 0.0f, w1 = 0.0f, a2 = 0.0f, w2 = 0.0f;   // chunks kb and kb + 1
             if (k1 > k0) {
-                load4(k0, na, nw);
-                cs = make_float4(na.x * nw.x, na.y * nw.y, na.z * nw.z, na.w * nw.w);
-                load4(k0 + 4, na, nw);
+                a1 = ld_sa(k0);
+                w1 = ld_sw(k0);
+                if (!kFused) {
+                    a2 = ld_sa(k0 + 1);
+                    w2 = ld_sw(k0 + 1);
+                }
             }
 #pragma unroll 1
             for (int kb = k0; kb < k1; ++kb, ++chunk) {
-                if (kb > k0 && ((kb - k0) & 3) == 0) {
-                    cs = make_float4(na.x * nw.x, na.y * nw.y, na.z * nw.z, na.w * nw.w);
-                    load4(kb + 4, na, nw);
+                float scale = a1 * w1;
+                if constexpr (kFused) {
+                    // One chunk ahead: only the weight scale is loaded here.
+                    w1 = ld_sw(kb + 1);
+                } else {
+                    a1 = a2;
+                    w1 = w2;
+                    a2 = ld_sa(kb + 2);
+                    w2 = ld_sw(kb + 2);
                 }
-                float scale = cs.x;
                 if constexpr (kFused) {
                     // The converter warps' scale of this row and chunk; the
                     // product is formed in the same order as sa * sw above.
@@ -738,16 +818,87 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(smem_addr(&sm.sa_empty[ring]));
-                    scale = sa_v * cs.x;
+                    scale = sa_v * scale;
                 }
                 if (!promote(chunk, scale, acc)) {
                     ok = false;
                     break;
                 }
-                cs = make_float4(cs.y, cs.z, cs.w, 0.0f);
             }
             if (!ok)
                 break;
+
+            if (kSplit && work.split > 1 && t >= work.full_end) {
+                // A piece of a split tile. It is the unit's last work, so
+                // the pipeline's stage memory is idle (every chunk's MMA has
+                // completed); each promotion warp stages its 16 KB of the
+                // partial tile there (float4 columns interleaved by lane) and
+                // moves it with one bulk copy.
+                static_assert(8 * 32 * (C::kCols / 4) * 16 <= C::kStages * C::kStageBytes, "staging");
+                const int tl = t - work.full_end;
+                constexpr uint32_t kWarpBytes = 32 * (C::kCols / 4) * 16;
+                float4* stage = reinterpret_cast<float4*>(&sm.a[0][0] + (warp - 4) * kWarpBytes);
+                auto part_of = [&](int j) {
+                    const size_t slot = static_cast<size_t>(tl) * (work.split - 1) + (j - 1);
+                    return reinterpret_cast<float4*>(p.sk_part) +
+                           ((slot * kCtas + rank) * 8 + (warp - 4)) * (C::kCols / 4) * 32;
+                };
+                auto flag_of = [&](int j) {
+                    const size_t slot = static_cast<size_t>(tl) * (work.split - 1) + (j - 1);
+                    return p.sk_flag + (slot * kCtas + rank) * 8 + (warp - 4);
+                };
+                if (work.cur > 0) {
+                    // Hand the partial to the tile's owner: shared memory,
+                    // one bulk copy to the workspace, then this warp's flag
+                    // set to the launch's epoch (release).
+#pragma unroll
+                    for (int i = 0; i < C::kCols / 4; ++i)
+                        stage[i * 32 + lane] =
+                            make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        bulk_store(part_of(work.cur), smem_addr(stage), kWarpBytes);
+                        bulk_commit_and_wait();
+                        fence_proxy_async_global();
+                        __threadfence();
+                        st_release_gpu(flag_of(work.cur), p.epoch);
+                    }
+                    __syncwarp();
+                    continue;
+                }
+                // The owner (piece 0) adds the other pieces in piece order,
+                // each brought into shared memory by one bulk copy.
+                const uint32_t bar = smem_addr(&sm.part_bar[warp - 4]);
+                for (int j = 1; j < work.split; ++j) {
+                    unsigned int* flag = flag_of(j);
+                    bool got = wait_flag(flag, p.epoch, abort_flag, p.err, p.wait_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, kWarpBytes);
+                        bulk_load(smem_addr(stage), part_of(j), kWarpBytes, bar);
+                    }
+                    got = mbar_wait(bar, (j - 1) & 1u, abort_flag, p.err, p.wait_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int i = 0; i < C::kCols / 4; ++i) {
+                        const float4 v = stage[i * 32 + lane];
+                        acc[2 * i] = make_float2(acc[2 * i].x + v.x, acc[2 * i].y + v.y);
+                        acc[2 * i + 1] = make_float2(acc[2 * i + 1].x + v.z, acc[2 * i + 1].y + v.w);
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        *flag = 0u;   // ready for the next launch that uses the workspace
+                }
+                if (!ok)
+                    break;
+            }
 
             // Epilogue through the warp's staging buffer: each thread writes
             // 64 bytes of its own row, then every store instruction writes 8
@@ -862,6 +1013,56 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 std::atomic<long long> g_stall_chunk{-1};
 std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 
+// Per-device launch counter: each launch that splits tiles marks its partial
+// tiles with a fresh nonzero epoch, so a flag left by an earlier (or
+// aborted) launch never matches.
+std::atomic<unsigned int> g_epoch[64];
+
+// K chunks per piece of a split tile, at least: handing a partial tile over
+// costs about as much as 2-3 chunks (measured on B300), so shorter pieces
+// lose more than the balance gains.
+constexpr int kMinPieceChunks = 16;
+
+inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// How the last wave of a dense launch is split: with T tiles on `units`
+// work units, the R = T mod units tiles of the last, partial wave are each
+// cut into S = min(units / R, KB / kMinPieceChunks) K ranges (S >= 2), so
+// that every unit has work in the last round. Workspace: one FP32 partial
+// tile per CTA for each piece after the first, then one flag per promotion
+// warp.
+struct SplitPlan {
+    int tiles = 0;
+    int split = 1;
+    size_t part_bytes = 0;
+    size_t bytes = 0;
+};
+
+template <int kCtas, int kBN>
+SplitPlan split_plan(int64_t rows, int64_t N, int64_t K, int64_t units)
+{
+    using C = Cfg<kCtas, kBN>;
+    SplitPlan sp;
+    const int64_t KB = K / BK;
+    const int64_t T = ((rows + C::kTileRows - 1) / C::kTileRows) * ((N + kBN - 1) / kBN);
+    if (units <= 0 || T <= 0 || KB < 2 * kMinPieceChunks)
+        return sp;
+    const int64_t R = T % units;
+    if (R == 0)
+        return sp;
+    int64_t S = units / R;
+    if (S > KB / kMinPieceChunks)
+        S = KB / kMinPieceChunks;
+    if (S < 2)
+        return sp;
+    sp.tiles = static_cast<int>(R);
+    sp.split = static_cast<int>(S);
+    const size_t slots = static_cast<size_t>(R) * static_cast<size_t>(S - 1);
+    sp.part_bytes = slots * kCtas * BM * kBN * sizeof(float);
+    sp.bytes = align256(sp.part_bytes) + slots * kCtas * C::kPromo * sizeof(unsigned int);
+    return sp;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -916,7 +1117,7 @@ bool encode_bf16_halves(CUtensorMap* map, const void* base, int64_t rows, int64_
 
 // Per device and shape: the dynamic shared-memory opt-in and the number of
 // work units (CTAs, or CTA pairs, which must share a GPC) resident at once.
-template <int kCtas, int kBN, bool kFused = false>
+template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
 fp8bs_status configure_once(int device, int sm_count, int* max_units)
 {
     constexpr int kThreads = Cfg<kCtas, kBN, kFused>::kThreads;
@@ -926,8 +1127,18 @@ fp8bs_status configure_once(int device, int sm_count, int* max_units)
     if (device < 0 || device >= 64)
         return FP8BS_ERR_CUDA;
     if (units[device] == 0) {
-        const auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused>;
+        using C = Cfg<kCtas, kBN, kFused>;
+        const auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused, kSplit>;
         const size_t smem = smem_bytes<kCtas, kBN, kFused>();
+        // setmaxnreg.inc waits until the CTA's register pool can grant the
+        // request, so the split must fit in what the kernel is launched with.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        if (fa.numRegs * kThreads < C::kCtrlRegs * C::kCtrlThreads + C::kEpilogueRegs * 32 * C::kPromo)
+            return FP8BS_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess) {
             cudaGetLastError();
@@ -966,9 +1177,25 @@ fp8bs_status configure_once(int device, int sm_count, int* max_units)
 // tiles.
 // kFused: a points at bf16 activations with row stride lda (elements);
 // otherwise at E4M3 codes with row stride K.
+// Work units (CTAs, or CTA pairs) a launch of `tile_bound` tiles at most
+// runs on.
+template <int kCtas, int kBN, bool kFused = false>
+fp8bs_status launch_units(const DeviceInfo& info, int64_t tile_bound, int64_t* units)
+{
+    int max_units = 0;
+    const fp8bs_status st = configure_once<kCtas, kBN, kFused>(info.device, info.sm_count, &max_units);
+    if (st != FP8BS_OK)
+        return st;
+    *units = tile_bound < max_units ? tile_bound : max_units;
+    return FP8BS_OK;
+}
+
+// ws / ws_bytes: workspace for splitting the last wave (dense launches only;
+// nullptr: no split).
 template <int kCtas, int kBN, bool kFused = false>
 fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_rows, Params p,
-                    int64_t K, cudaStream_t stream, int64_t lda = 0)
+                    int64_t K, cudaStream_t stream, int64_t lda = 0, void* ws = nullptr,
+                    size_t ws_bytes = 0)
 {
     using C = Cfg<kCtas, kBN, kFused>;
     constexpr int kThreads = C::kThreads;
@@ -994,14 +1221,36 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
         if (!a_ok || !encode_operand(&map_b, qw, w_rows, K, C::kBRows))
             return FP8BS_ERR_CUDA;
     }
-    int max_units = 0;
-    st = configure_once<kCtas, kBN, kFused>(info.device, info.sm_count, &max_units);
+    int64_t units64 = 0;
+    st = launch_units<kCtas, kBN, kFused>(info, tile_bound, &units64);
     if (st != FP8BS_OK)
         return st;
-    const auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused>;
-    const int units = static_cast<int>(tile_bound < max_units ? tile_bound : max_units);
+    auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused, false>;
+    const int units = static_cast<int>(units64);
     if (units <= 0)
         return FP8BS_OK;
+    if constexpr (!kFused) {
+        if (ws != nullptr && p.offsets == nullptr) {
+            const SplitPlan sp = split_plan<kCtas, kBN>(rows, p.N, K, units);
+            if (sp.tiles > 0) {
+                if (ws_bytes < sp.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+                    return FP8BS_ERR_INVALID_ARG;
+                unsigned int e = g_epoch[info.device].fetch_add(1) + 1;
+                if (e == 0)
+                    e = g_epoch[info.device].fetch_add(1) + 1;
+                p.sk_tiles = sp.tiles;
+                p.sk_split = sp.split;
+                p.sk_part = static_cast<float*>(ws);
+                p.sk_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes));
+                p.epoch = e;
+                int split_units = 0;
+                st = configure_once<kCtas, kBN, false, true>(info.device, info.sm_count, &split_units);
+                if (st != FP8BS_OK)
+                    return st;
+                kernel = fp8_gemm_kernel<kCtas, kBN, false, true>;
+            }
+        }
+    }
     // Programmatic dependent launch: the kernel's set-up may overlap the tail
     // of the previous kernel in the stream (it waits for that kernel's
     // results before its first global-memory access).
@@ -1068,23 +1317,59 @@ Params make_params(const float* sa, const float* sw, void* c, fp8bs_out_dtype ou
 }
 
 // Tile shape of a launch (fp8bs_tile without AUTO): CTAs per MMA and tile
-// width. Single CTA, 128 x 256 tiles is the automatic choice: on B300 it is
-// the fastest or within run-to-run noise of the fastest shape across the
-// dense and MoE workloads, and it needs no cluster co-scheduling. A 256-wide
-// tile needs N % 256 == 0 to be fully used; other N take 128-wide tiles.
-fp8bs_tile auto_tile(int64_t N)
+// width. Measured on B300: for dense GEMMs the CTA pair's 256 x 256 tile is
+// as fast as 128 x 256 at K = 7168 and 8 % faster at K = 2048 (each CTA
+// stages half of the W tile, so it loads a third less per chunk); for the
+// MoE grouped GEMM, whose experts hold few rows, the 128-row tile wastes
+// less and is 25 % faster. A 256-wide tile needs N % 256 == 0 to be fully
+// used; other N take 128-wide tiles.
+fp8bs_tile auto_tile(int64_t N, int64_t M, bool grouped)
 {
-    return N % 256 == 0 ? FP8BS_TILE_128x256 : FP8BS_TILE_128x128;
+    if (N % 256 != 0)
+        return FP8BS_TILE_128x128;
+    return grouped || M <= 128 ? FP8BS_TILE_128x256 : FP8BS_TILE_PAIR_256x256;
 }
 
 fp8bs_status launch_tile(fp8bs_tile tile, const uint8_t* qa, int64_t rows, const uint8_t* qw,
-                         int64_t w_rows, const Params& p, int64_t K, cudaStream_t s)
+                         int64_t w_rows, const Params& p, int64_t K, cudaStream_t s, void* ws = nullptr,
+                         size_t ws_bytes = 0)
 {
     switch (tile) {
-    case FP8BS_TILE_128x256: return launch<1, 256>(qa, rows, qw, w_rows, p, K, s);
-    case FP8BS_TILE_128x128: return launch<1, 128>(qa, rows, qw, w_rows, p, K, s);
-    case FP8BS_TILE_PAIR_256x256: return launch<2, 256>(qa, rows, qw, w_rows, p, K, s);
-    case FP8BS_TILE_PAIR_256x128: return launch<2, 128>(qa, rows, qw, w_rows, p, K, s);
+    case FP8BS_TILE_128x256: return launch<1, 256>(qa, rows, qw, w_rows, p, K, s, 0, ws, ws_bytes);
+    case FP8BS_TILE_128x128: return launch<1, 128>(qa, rows, qw, w_rows, p, K, s, 0, ws, ws_bytes);
+    case FP8BS_TILE_PAIR_256x256: return launch<2, 256>(qa, rows, qw, w_rows, p, K, s, 0, ws, ws_bytes);
+    case FP8BS_TILE_PAIR_256x128: return launch<2, 128>(qa, rows, qw, w_rows, p, K, s, 0, ws, ws_bytes);
+    default: break;
+    }
+    return FP8BS_ERR_INVALID_ARG;
+}
+
+// Workspace bytes a dense launch of this shape and tile needs to split its
+// last wave (0: it does not split).
+template <int kCtas, int kBN>
+fp8bs_status plan_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes)
+{
+    using C = Cfg<kCtas, kBN>;
+    DeviceInfo info;
+    fp8bs_status st = require_sm103(&info);
+    if (st != FP8BS_OK)
+        return st;
+    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    int64_t units = 0;
+    st = launch_units<kCtas, kBN>(info, (M / C::kTileRows + 1) * n_tiles, &units);
+    if (st != FP8BS_OK)
+        return st;
+    *bytes = split_plan<kCtas, kBN>(M, N, K, units).bytes;
+    return FP8BS_OK;
+}
+
+fp8bs_status tile_plan_bytes(fp8bs_tile tile, int64_t M, int64_t N, int64_t K, size_t* bytes)
+{
+    switch (tile) {
+    case FP8BS_TILE_128x256: return plan_bytes<1, 256>(M, N, K, bytes);
+    case FP8BS_TILE_128x128: return plan_bytes<1, 128>(M, N, K, bytes);
+    case FP8BS_TILE_PAIR_256x256: return plan_bytes<2, 256>(M, N, K, bytes);
+    case FP8BS_TILE_PAIR_256x128: return plan_bytes<2, 128>(M, N, K, bytes);
     default: break;
     }
     return FP8BS_ERR_INVALID_ARG;
@@ -1126,8 +1411,48 @@ extern "C" fp8bs_status fp8bs_gemm_tiled(const uint8_t* qa, const float* sa, con
     if (M > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
     const Params p = make_params(sa, sw, c, out_dtype, M, N, K, ldc, nullptr, 1);
-    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N) : tile, qa, M, qw, N, p, K,
+    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N, M, false) : tile, qa, M, qw, N, p, K,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8bs_tile tile,
+                                                  size_t* bytes)
+{
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (K % BK != 0 || N % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    if (!valid_tile(tile, N))
+        return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || K == 0)
+        return FP8BS_OK;
+    if (M > 0x7FFFFFFF || N > (int64_t(1) << 24) || K > (int64_t(1) << 31) - BK)
+        return FP8BS_ERR_UNSUPPORTED;
+    return tile_plan_bytes(tile == FP8BS_TILE_AUTO ? auto_tile(N, M, false) : tile, M, N, K, bytes);
+}
+
+extern "C" fp8bs_status fp8bs_gemm_ws(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                      const float* sw, void* c, fp8bs_out_dtype out_dtype, int64_t M,
+                                      int64_t N, int64_t K, int64_t ldc, fp8bs_tile tile,
+                                      void* workspace, size_t workspace_bytes, fp8bs_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % BK != 0 || N % 128 != 0)
+        return FP8BS_ERR_UNSUPPORTED;
+    if (!valid_tile(tile, N))
+        return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    fp8bs_status st = check_common(qa, sa, qw, sw, c, out_dtype, N, K, ldc);
+    if (st != FP8BS_OK)
+        return st;
+    if (M > 0x7FFFFFFF)
+        return FP8BS_ERR_UNSUPPORTED;
+    const Params p = make_params(sa, sw, c, out_dtype, M, N, K, ldc, nullptr, 1);
+    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N, M, false) : tile, qa, M, qw, N, p, K,
+                       reinterpret_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
 extern "C" fp8bs_status fp8bs_gemm(const uint8_t* qa, const float* sa, const uint8_t* qw,
@@ -1161,7 +1486,7 @@ extern "C" fp8bs_status fp8bs_grouped_gemm_tiled(const uint8_t* qa, const float*
     if (total_M > 0x7FFFFFFF || static_cast<int64_t>(E) * N > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
     const Params p = make_params(sa, sw, c, out_dtype, total_M, N, K, ldc, expert_offsets, E);
-    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N) : tile, qa, total_M, qw,
+    return launch_tile(tile == FP8BS_TILE_AUTO ? auto_tile(N, total_M, true) : tile, qa, total_M, qw,
                        static_cast<int64_t>(E) * N, p, K, reinterpret_cast<cudaStream_t>(stream));
 }
 

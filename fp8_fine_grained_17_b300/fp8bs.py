@@ -78,6 +78,11 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_last_device_error.argtypes = [vp]
         L.fp8bs_last_device_error.restype = st
+        L.fp8bs_gemm_ws.argtypes = [vp, f32p, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64,
+                                    ctypes.c_int, vp, ctypes.c_size_t, vp]
+        L.fp8bs_gemm_ws.restype = st
+        L.fp8bs_gemm_workspace_size.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+        L.fp8bs_gemm_workspace_size.restype = st
         L.fp8bs_test_inject_stall.argtypes = [i64, i64]
         L.fp8bs_test_inject_stall.restype = st
         _lib = L
@@ -203,6 +208,28 @@ def fp8bs_gemm(qa, sa, qw, sw, c, stream=None, tile=TILE_AUTO):
         _check("fp8bs_gemm_tiled", lib().fp8bs_gemm_tiled(*args, int(tile), _stream(stream)))
 
 
+def fp8bs_gemm_workspace_size(M: int, N: int, K: int, tile=TILE_AUTO) -> int:
+    """Workspace bytes fp8bs_gemm_ws needs on the current device (0: no split)."""
+    n = ctypes.c_size_t(0)
+    _check("fp8bs_gemm_workspace_size",
+           lib().fp8bs_gemm_workspace_size(int(M), int(N), int(K), int(tile), ctypes.byref(n)))
+    return int(n.value)
+
+
+def fp8bs_gemm_ws(qa, sa, qw, sw, c, workspace, stream=None, tile=TILE_AUTO):
+    """fp8bs_gemm with a workspace (uint8 CUDA tensor, zero-filled before its
+    first use, or None) that lets the last wave of tiles be split along K."""
+    M, K = qa.shape
+    N = qw.shape[0]
+    for t in (qa, sa, qw, sw):
+        assert t.is_contiguous()
+    ws = _ptr(workspace) if workspace is not None else None
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("fp8bs_gemm_ws", lib().fp8bs_gemm_ws(_ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw), _ptr(c),
+                                                _out_dtype(c), M, N, K, _row_stride(c), int(tile), ws,
+                                                nbytes, _stream(stream)))
+
+
 def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None, tile=TILE_AUTO):
     """Per expert e: rows offsets[e]:offsets[e+1] of A times W_e^T."""
     total_M, K = qa.shape
@@ -290,6 +317,18 @@ def quantize_weight(w: torch.Tensor, stream=None, pow2: bool = False):
 def gemm(qa, sa, qw, sw, out_dtype=torch.bfloat16, stream=None, tile=TILE_AUTO):
     c = torch.empty((qa.shape[0], qw.shape[0]), dtype=out_dtype, device=qa.device)
     fp8bs_gemm(qa, sa, qw, sw, c, stream, tile)
+    return c
+
+
+def workspace(M: int, N: int, K: int, tile=TILE_AUTO, device=None):
+    """A zero-filled workspace for fp8bs_gemm_ws (None when the shape needs none)."""
+    n = fp8bs_gemm_workspace_size(M, N, K, tile)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda") if n else None
+
+
+def gemm_ws(qa, sa, qw, sw, ws, out_dtype=torch.bfloat16, stream=None, tile=TILE_AUTO):
+    c = torch.empty((qa.shape[0], qw.shape[0]), dtype=out_dtype, device=qa.device)
+    fp8bs_gemm_ws(qa, sa, qw, sw, c, ws, stream, tile)
     return c
 
 

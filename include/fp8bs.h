@@ -49,6 +49,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -70,9 +71,10 @@ typedef enum { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 } fp8bs_out_dtype;
 
 /*
  * Output tile of the GEMM kernels (all give identical results; they differ
- * only in speed). AUTO picks 128x256 when N % 256 == 0, else 128x128. The
- * PAIR shapes run a CTA pair (thread-block cluster of 2) per tile with the
- * pair-wide tensor-core MMA; PAIR_256x256 needs N % 256 == 0.
+ * only in speed). AUTO picks, when N % 256 == 0, PAIR_256x256 for dense
+ * GEMMs with M > 128 and 128x256 for grouped GEMMs and M <= 128; else
+ * 128x128. The PAIR shapes run a CTA pair (thread-block cluster of 2) per
+ * tile with the pair-wide tensor-core MMA; PAIR_256x256 needs N % 256 == 0.
  */
 typedef enum {
     FP8BS_TILE_AUTO = 0,
@@ -211,6 +213,46 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *qa, const float *sa, const uint8_t 
                               const float *sw, void *c, fp8bs_out_dtype out_dtype, int64_t M,
                               int64_t N, int64_t K, int64_t ldc, fp8bs_tile tile,
                               fp8bs_stream_t stream);
+
+/*
+ * fp8bs_gemm with a workspace that lets the GEMM balance its last wave of
+ * output tiles. The kernel runs one work unit (a CTA, or a CTA pair for the
+ * PAIR tiles) per SM and deals the tiles out round by round; when the tile
+ * count is not a multiple of the unit count, the last round would leave most
+ * units idle. With a workspace, each tile of that last round is instead cut
+ * into S ranges of K chunks (S = min(units / tiles left, K / 2048), at least 2)
+ * computed by different units: the owner of a tile (the unit with its first
+ * range) adds the others' FP32 partial tiles, in range order, after its own
+ * chunks, and stores C. Same output, same accuracy bound as fp8bs_gemm; the
+ * bits of split tiles may differ from fp8bs_gemm's (the K sum is grouped
+ * differently), but a given shape, tile and device always gives the same
+ * bits.
+ *
+ *   workspace        DEVICE memory of at least the size
+ *                    fp8bs_gemm_workspace_size reports, 256-byte aligned,
+ *                    zero-filled before its first use (the kernel leaves it
+ *                    reusable: flags it consumes are reset to zero). NULL:
+ *                    no split (exactly fp8bs_gemm_tiled).
+ *   workspace_bytes  its size; too small: FP8BS_ERR_INVALID_ARG.
+ * Two launches that use the same workspace at the same time on the GPU
+ * (different streams) race; launches in one stream do not. The other
+ * arguments are those of fp8bs_gemm_tiled. The library still allocates
+ * nothing.
+ */
+fp8bs_status fp8bs_gemm_ws(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
+                           void *c, fp8bs_out_dtype out_dtype, int64_t M, int64_t N, int64_t K,
+                           int64_t ldc, fp8bs_tile tile, void *workspace, size_t workspace_bytes,
+                           fp8bs_stream_t stream);
+
+/*
+ * Workspace bytes fp8bs_gemm_ws needs for this shape and tile on the current
+ * device (0 when no wave is split: the tile count is a multiple of the units,
+ * K < 4096, or the problem fits in one partial wave). At most one FP32
+ * 128 x 256 (or 128 x 128) tile per SM plus 32 bytes of flags per SM. Same
+ * argument checks as fp8bs_gemm_tiled; bytes must not be NULL.
+ */
+fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8bs_tile tile,
+                                       size_t *bytes);
 
 /*
  * Grouped (MoE) GEMM: for each expert e, rows r in

@@ -206,3 +206,105 @@ def test_back_to_back_steps_share_code_buffers():
     assert not torch.equal(refs[0], refs[1])
     for i, c in enumerate(outs):
         assert torch.equal(c, refs[i % 2]), f"step {i}"
+
+
+# Shapes whose last wave is split on a 148-SM B300 (pieces of at least 16
+# K chunks): CTA pair 2048 x 3328 x 4096 (104 tiles on 74 pairs: 30 tiles in
+# 2 pieces), 128x256 1024 x 5888 x 4096 (184 tiles on 148 CTAs: 36 tiles in
+# 2 pieces), 128x128 1000 x 3072 x 6144 (192 tiles: 44 tiles in 3 pieces,
+# with a partial row tile).
+SPLIT_CASES = [(2048, 3328, 4096, fp8bs.TILE_PAIR_256x256), (1024, 5888, 4096, fp8bs.TILE_128x256),
+               (1000, 3072, 6144, fp8bs.TILE_128x128)]
+
+
+@pytest.mark.parametrize("M,N,K,tile", SPLIT_CASES)
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_split_wave_against_oracle(orc, M, N, K, tile, out):
+    rng = np.random.default_rng(M + N + K + tile)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = gpu_quant_act(a)
+    qw, sw = gpu_quant_weight(w)
+    nbytes = fp8bs.fp8bs_gemm_workspace_size(M, N, K, tile)
+    assert nbytes > 0, "this shape is meant to split its last wave"
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    c = fp8bs.gemm_ws(qa, sa, qw, sw, ws, out, tile=tile)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
+    check_gemm(c, C_or, B, out == torch.bfloat16)
+    # Deterministic: the same call again (workspace reused) gives the same bits.
+    c2 = fp8bs.gemm_ws(qa, sa, qw, sw, ws, out, tile=tile)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    assert torch.equal(c.view(torch.int16 if out == torch.bfloat16 else torch.int32),
+                       c2.view(torch.int16 if out == torch.bfloat16 else torch.int32))
+    # No workspace: exactly fp8bs_gemm.
+    c3 = fp8bs.gemm_ws(qa, sa, qw, sw, None, out, tile=tile)
+    c4 = fp8bs.gemm(qa, sa, qw, sw, out, tile=tile)
+    assert torch.equal(c3, c4)
+
+
+def test_split_wave_workspace_checks():
+    M, N, K, tile = SPLIT_CASES[0]
+    nbytes = fp8bs.fp8bs_gemm_workspace_size(M, N, K, tile)
+    qa = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((M, K // 128), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    small = torch.zeros(nbytes - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp8bs.Fp8bsError):
+        fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, small, tile=tile)
+    big = torch.zeros(nbytes + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp8bs.Fp8bsError):   # not 256-byte aligned
+        fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, big[16:], tile=tile)
+    # Shapes that do not split need no workspace (too few K chunks to cut).
+    assert fp8bs.fp8bs_gemm_workspace_size(256, 256, 1024, fp8bs.TILE_128x256) == 0
+    assert fp8bs.fp8bs_gemm_workspace_size(4096, 7168, 2048, fp8bs.TILE_PAIR_256x256) == 0
+
+
+@pytest.mark.slow
+def test_full_workload_split_wave(orc):
+    """The 4096 x 4096 x 7168 workload through fp8bs_gemm_ws with the
+    automatic tile (its last wave split): every output element against the
+    oracle."""
+    d = wl.cfg3(0)
+    M, K = d.a_bits.shape
+    N = d.w_bits.shape[0]
+    qa, sa = gpu_quant_act(d.a_bits)
+    qw, sw = gpu_quant_weight(d.w_bits)
+    ws = fp8bs.workspace(M, N, K)
+    assert ws is not None
+    c = fp8bs.gemm_ws(qa, sa, qw, sw, ws, torch.bfloat16)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(d.a_bits), *orc.quantize_weight_128x128(d.w_bits))
+    worst = check_gemm(c, C_or, B, True)
+    print(f"4096x4096x7168 split wave: worst err/tol = {worst:.3g}")
+
+
+def test_split_wave_back_to_back_launches():
+    """Launches of the headline shape back to back on one stream, sharing one
+    workspace and alternating two input sets, with no host sync: each output
+    equals the same launch run alone (the flags of one launch never release
+    the next one's owners early)."""
+    M, N, K = 4096, 4096, 7168
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    sets = []
+    for _ in range(2):
+        qa = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+        qw = torch.randint(0, 0x7E, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+        sa = torch.rand((M, K // 128), device="cuda", generator=g) * 1e-2
+        sw = torch.rand((N // 128, K // 128), device="cuda", generator=g) * 1e-2
+        sets.append((qa, sa, qw, sw))
+    ws = fp8bs.workspace(M, N, K)
+    refs = []
+    for s in sets:
+        refs.append(fp8bs.gemm_ws(*s, ws, torch.bfloat16))
+        torch.cuda.synchronize()
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    for i, c in enumerate(outs):
+        fp8bs.fp8bs_gemm_ws(*sets[i % 2], c, ws)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    for i, c in enumerate(outs):
+        assert torch.equal(c, refs[i % 2]), f"launch {i}"
