@@ -1572,3 +1572,69 @@ extern "C" fp8bs_status fp8bs_test_inject_stall(int64_t chunk, int64_t wait_limi
     g_stall_chunk.store(chunk);
     return FP8BS_OK;
 }
+
+// ----------------------------------------------------------------------------
+// Allocation-free variant of fp8bs_gemm_ws, for callers that cannot allocate
+// device memory at the point of the call (an allocator that must not be
+// re-entered from inside a callback, a plug-in that may not own memory, code
+// that runs where a cudaMalloc would synchronize or fail). Its workspace is
+// this file-scope array: every GPU that loads the library holds it until the
+// process exits, and every call on a device shares it.
+namespace fp8bs {
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(12) << 20;   // 12 MiB
+// Zero at load. The kernel needs no part of it cleared per call: a flag
+// counts only when it holds the launch's own epoch (a per-device counter
+// that never repeats a value in practice), and owners reset the flags they
+// consume; the partial tiles are always written before they are read.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64];
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) and cached.
+fp8bs_status noalloc_scratch(const DeviceInfo& info, void** out)
+{
+    if (info.device < 0 || info.device >= 64)
+        return FP8BS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[info.device] == nullptr) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        g_noalloc_addr[info.device] = ptr;
+    }
+    *out = g_noalloc_addr[info.device];
+    return FP8BS_OK;
+}
+}  // namespace
+}  // namespace fp8bs
+
+extern "C" fp8bs_status fp8bs_gemm_noalloc(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                           const float* sw, void* c, fp8bs_out_dtype out_dtype,
+                                           int64_t M, int64_t N, int64_t K, int64_t ldc,
+                                           fp8bs_tile tile, fp8bs_stream_t stream)
+{
+    size_t need = 0;
+    fp8bs_status st = fp8bs_gemm_workspace_size(M, N, K, tile, &need);
+    if (st != FP8BS_OK)
+        return st;
+    if (need > kNoAllocScratchBytes)
+        return FP8BS_ERR_UNSUPPORTED;   // this shape's split needs more than the fixed scratch
+    void* ws = nullptr;
+    if (need > 0) {
+        DeviceInfo info;
+        st = require_sm103(&info);
+        if (st != FP8BS_OK)
+            return st;
+        st = noalloc_scratch(info, &ws);
+        if (st != FP8BS_OK)
+            return st;
+    }
+    return fp8bs_gemm_ws(qa, sa, qw, sw, c, out_dtype, M, N, K, ldc, tile, ws,
+                         need > 0 ? kNoAllocScratchBytes : 0, stream);
+}

@@ -23,6 +23,7 @@ OUT_F32, OUT_BF16 = 0, 1
 TILE_AUTO, TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128 = 0, 1, 2, 3, 4
 TILES = (TILE_128x256, TILE_128x128, TILE_PAIR_256x256, TILE_PAIR_256x128)
 NORM_RMS, NORM_LAYER = 0, 1
+NOALLOC_SCRATCH_BYTES = 12 << 20   # FP8BS_NOALLOC_SCRATCH_BYTES in include/fp8bs.h
 
 
 class Fp8bsError(RuntimeError):
@@ -83,6 +84,9 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_gemm_ws.restype = st
         L.fp8bs_gemm_workspace_size.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
         L.fp8bs_gemm_workspace_size.restype = st
+        L.fp8bs_gemm_noalloc.argtypes = [vp, f32p, vp, f32p, vp, ctypes.c_int, i64, i64, i64, i64,
+                                         ctypes.c_int, vp]
+        L.fp8bs_gemm_noalloc.restype = st
         L.fp8bs_test_inject_stall.argtypes = [i64, i64]
         L.fp8bs_test_inject_stall.restype = st
         _lib = L
@@ -228,6 +232,18 @@ def fp8bs_gemm_ws(qa, sa, qw, sw, c, workspace, stream=None, tile=TILE_AUTO):
     _check("fp8bs_gemm_ws", lib().fp8bs_gemm_ws(_ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw), _ptr(c),
                                                 _out_dtype(c), M, N, K, _row_stride(c), int(tile), ws,
                                                 nbytes, _stream(stream)))
+
+
+def fp8bs_gemm_noalloc(qa, sa, qw, sw, c, stream=None, tile=TILE_AUTO):
+    """fp8bs_gemm_ws with the library's fixed device scratch as workspace:
+    nothing is allocated by the call (for callers that cannot allocate)."""
+    M, K = qa.shape
+    N = qw.shape[0]
+    for t in (qa, sa, qw, sw):
+        assert t.is_contiguous()
+    _check("fp8bs_gemm_noalloc", lib().fp8bs_gemm_noalloc(_ptr(_u8(qa)), _ptr(sa), _ptr(_u8(qw)), _ptr(sw),
+                                                          _ptr(c), _out_dtype(c), M, N, K, _row_stride(c),
+                                                          int(tile), _stream(stream)))
 
 
 def fp8bs_grouped_gemm(qa, sa, expert_offsets, qw, sw, c, stream=None, tile=TILE_AUTO):

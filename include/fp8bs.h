@@ -255,6 +255,34 @@ fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, fp8bs_ti
                                        size_t *bytes);
 
 /*
+ * fp8bs_gemm_ws for callers that cannot allocate device memory where they
+ * call the GEMM: for example an allocator or memory-pool callback that must
+ * not re-enter the allocator, a plug-in that may not own device memory, or
+ * code on a path where cudaMalloc would synchronize the device or fail. The
+ * pages describe no such call; it is an addition of this library.
+ *
+ * The workspace is a fixed 12 MiB (FP8BS_NOALLOC_SCRATCH_BYTES) array in the
+ * library's own device memory: every GPU that loads the library holds it
+ * until the process exits, and all calls on a device share it. The call
+ * allocates and frees nothing (no cudaMalloc, no allocating library call).
+ * Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it, so make that first call before any
+ * stream capture. Calls whose executions overlap on the GPU (different
+ * streams, or threads racing on one device) race on the shared array; calls
+ * in one stream do not. A shape whose split needs more than the array
+ * (fp8bs_gemm_workspace_size > FP8BS_NOALLOC_SCRATCH_BYTES) is rejected with
+ * FP8BS_ERR_UNSUPPORTED before anything is launched; shapes that do not
+ * split use no workspace. Arguments, results and accuracy are those of
+ * fp8bs_gemm_ws; the bits equal fp8bs_gemm_ws's with any large enough
+ * workspace.
+ */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (12u << 20)
+fp8bs_status fp8bs_gemm_noalloc(const uint8_t *qa, const float *sa, const uint8_t *qw,
+                                const float *sw, void *c, fp8bs_out_dtype out_dtype, int64_t M,
+                                int64_t N, int64_t K, int64_t ldc, fp8bs_tile tile,
+                                fp8bs_stream_t stream);
+
+/*
  * Grouped (MoE) GEMM: for each expert e, rows r in
  * [expert_offsets[e], expert_offsets[e+1]) of A are multiplied by W_e:
  * C[r, :] = A_hat[r, :] * W_hat_e^T.
