@@ -3,6 +3,8 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "fp8bs_device.cuh"
 #include "fp8bs_host.h"
 
@@ -36,6 +38,23 @@ unsigned int* device_error_word()
         g_err_ptr[dev] = static_cast<unsigned int*>(p);
     }
     return g_err_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
 }
 
 bool current_device(DeviceInfo* out)

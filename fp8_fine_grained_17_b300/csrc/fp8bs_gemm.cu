@@ -1063,23 +1063,6 @@ SplitPlan split_plan(int64_t rows, int64_t N, int64_t K, int64_t units)
     return sp;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 // K-major FP8 operand [rows, K] (row stride K bytes), box 128 (K) x box_rows.
 bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows)
 {

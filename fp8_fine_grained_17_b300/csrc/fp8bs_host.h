@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "fp8bs.h"
 
@@ -26,6 +27,10 @@ fp8bs_status require_sm103(DeviceInfo* info);
 // Device address of the library's error word on the current device (cached
 // per device); nullptr if the runtime cannot provide it.
 unsigned int* device_error_word();
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once;
+// nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder();
 
 inline bool aligned16(const void* p)
 {

@@ -8,6 +8,7 @@
 // codec (scale, reciprocal, codes) is in fp8bs_e4m3.cuh.
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "fp8bs_device.cuh"
@@ -119,78 +120,147 @@ quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* _
         act_regs_batch<kContiguous>(base, x, ldx, q, ldq, scale, groups_per_row, total_groups, pow2);
 }
 
-// Large contiguous inputs (ld == K, at least kTmaMinGroups groups): the
-// input is one stream of 256-byte groups. A CTA of 4 warps takes 128-group
-// chunks (32 KB) in a grid-stride order and keeps a 3-stage ring of them in
-// flight with bulk asynchronous copies (cp.async.bulk, mbarrier-tracked), so
-// the loads of the next two chunks are outstanding while one is quantized
-// from shared memory. For smaller inputs each CTA gets only a few chunks and
-// the ring's fill latency dominates; the register path is faster there
-// (measured on B300: [4096, 7168] 22.9 us register path vs 25.2 us ring;
-// [16384, 7168] 68.9 us vs 67.7 us).
-constexpr int kTmaThreads = 128;
-constexpr int kTmaChunkGroups = 128;
-constexpr int kTmaChunkBytes = kTmaChunkGroups * 256;
-constexpr int kTmaStages = 3;
-constexpr int64_t kTmaMinGroups = int64_t(1) << 19;
+// Ring kernel: a persistent grid of 4-warp CTAs (two per SM) that streams a
+// list of 32 KB work items through a 3-stage shared-memory ring, so that the
+// loads of the next two items are in flight while one is quantized. Items:
+//   activation chunks   128 consecutive 1x128 groups of a contiguous bf16
+//                       tensor (ld == K), brought in by one bulk copy;
+//   weight blocks       one 128x128 bf16 block, brought in by one 2-D TMA
+//                       tile load (rows past N read as zeros).
+// Item i of the grid's list goes to CTA i mod grid. The codec is the one of
+// the register paths (same codes and scales). Used for the activation
+// quantizer on large contiguous inputs and for the activation + weight pair
+// of a GEMM step (one launch, both lists back to back). Smaller inputs take
+// the register path, whose fill latency is lower (measured on B300:
+// [4096, 7168] 22.9 us register path vs 25.2 us ring).
+constexpr int kRingThreads = 128;
+constexpr int kRingItemGroups = 128;
+constexpr int kRingItemBytes = kRingItemGroups * 256;
+constexpr int kRingStages = 3;
+constexpr int64_t kRingMinGroups = int64_t(1) << 19;
 
-struct __align__(128) ActSmem {
-    uint8_t stage[kTmaStages][kTmaChunkBytes];
-    uint64_t full[kTmaStages];
+struct __align__(128) RingSmem {
+    uint8_t stage[kRingStages][kRingItemBytes];
+    uint64_t full[kRingStages];
+    uint32_t wmax[kRingThreads / 32];
     int abort;
 };
-constexpr size_t kActSmemBytes = sizeof(ActSmem) + 128;
+constexpr size_t kRingSmemBytes = sizeof(RingSmem) + 128;
 
-__global__ void __launch_bounds__(kTmaThreads)
-quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ q,
-                           float* __restrict__ scale, int64_t total_groups, unsigned int* err, int pow2)
+struct RingWork {
+    // activation chunks: items [0, n_act)
+    const uint16_t* x;
+    uint8_t* qx;
+    float* sx;
+    int64_t x_groups;
+    int64_t n_act;
+    // weight blocks: items [n_act, n_act + n_w); block (kb, nb) of item
+    // n_act + kb + nb * w_gpr
+    uint8_t* qw;
+    int64_t ldqw;
+    float* sw;
+    int64_t N;
+    int64_t w_gpr;
+    int64_t n_w;
+    unsigned int* err;
+    int pow2;
+};
+
+// Weight block from a stage (128 rows x 256 B, row-major): thread t holds the
+// 16-byte column chunk t & 15 of rows (t >> 4) + 8 i; block amax by a warp
+// max-reduction and the four warps' maxima, codes written per row.
+__device__ __forceinline__ void ring_weight_block(const uint8_t* stage, const RingWork& p, int64_t kb,
+                                                  int64_t nb, uint32_t* wmax)
+{
+    const int t = threadIdx.x;
+    const int c16 = t & 15;
+    const int r0 = t >> 4;
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + (r0 + 8 * i) * 256 + 16 * c16);
+        m = max(m, absmax_words(&v, 1));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((t & 31) == 0)
+        wmax[t >> 5] = m;
+    __syncthreads();
+    const uint32_t a = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
+    const Divider d = group_divider(a, p.pow2);
+    if (t == 0)
+        p.sw[nb * p.w_gpr + kb] = d.s;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const int64_t n = nb * 128 + r0 + 8 * i;
+        if (n < p.N) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + (r0 + 8 * i) * 256 + 16 * c16);
+            __stcs(reinterpret_cast<uint2*>(p.qw + n * p.ldqw + kb * 128 + 8 * c16), quantize8(v, d));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kRingThreads)
+quantize_ring_kernel(const __grid_constant__ CUtensorMap wmap, const RingWork p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
-    ActSmem& sm = *reinterpret_cast<ActSmem*>(smem_raw + (((raw + 127u) & ~127u) - raw));
+    RingSmem& sm = *reinterpret_cast<RingSmem*>(smem_raw + (((raw + 127u) & ~127u) - raw));
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t = lane & 3;
     const int quad_base = lane & ~3;
     const int rot = (lane >> 2) & 1;
-    const int64_t n_chunks = (total_groups + kTmaChunkGroups - 1) / kTmaChunkGroups;
+    const int64_t n_items = p.n_act + p.n_w;
 
+    // A GEMM launched after this kernel as its programmatic dependent may be
+    // scheduled once every CTA here is running; it waits for the results.
+    if (threadIdx.x == 0)
+        launch_dependents();
     auto issue = [&](int64_t c, int s) {
-        const int64_t g0 = c * kTmaChunkGroups;
-        const int64_t n = min(static_cast<int64_t>(kTmaChunkGroups), total_groups - g0);
         const uint32_t bar = smem_addr(&sm.full[s]);
-        const uint32_t bytes = static_cast<uint32_t>(n * 256);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(smem_addr(sm.stage[s]), x + g0 * 128, bytes, bar);
+        if (c < p.n_act) {
+            const int64_t g0 = c * kRingItemGroups;
+            const int64_t n = min(static_cast<int64_t>(kRingItemGroups), p.x_groups - g0);
+            const uint32_t bytes = static_cast<uint32_t>(n * 256);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(smem_addr(sm.stage[s]), p.x + g0 * 128, bytes, bar);
+        } else {
+            const int64_t wi = c - p.n_act;
+            mbar_arrive_expect_tx(bar, kRingItemBytes);
+            tma_load_2d(smem_addr(sm.stage[s]), &wmap, bar, static_cast<int32_t>((wi % p.w_gpr) * 128),
+                        static_cast<int32_t>((wi / p.w_gpr) * 128));
+        }
     };
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTmaStages; ++s)
+        for (int s = 0; s < kRingStages; ++s)
             mbar_init(smem_addr(&sm.full[s]), 1);
         sm.abort = 0;
         fence_barrier_init();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTmaStages; ++s) {
+        if (p.n_w > 0)
+            tma_prefetch_desc(&wmap);
+        for (int s = 0; s < kRingStages; ++s) {
             const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-            if (c < n_chunks)
+            if (c < n_items)
                 issue(c, s);
         }
     }
     int s = 0;
     uint32_t ph = 0;
-    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-        const bool ready = mbar_wait(smem_addr(&sm.full[s]), ph, &sm.abort, err);
+    for (int64_t c = blockIdx.x; c < n_items; c += gridDim.x) {
+        const bool ready = mbar_wait(smem_addr(&sm.full[s]), ph, &sm.abort, p.err);
         if (!__syncthreads_and(ready)) {
             // A wait gave up (reported in err): let the copies still in
             // flight land (bounded waits) before the CTA leaves.
             if (threadIdx.x == 0) {
                 int ds = s;
                 uint32_t dph = ph;
-                for (int i = 0; i < kTmaStages; ++i) {
-                    if (c + static_cast<int64_t>(i) * gridDim.x < n_chunks)
-                        mbar_wait_drain(smem_addr(&sm.full[ds]), dph, kWaitLimitNs, err);
-                    if (++ds == kTmaStages) {
+                for (int i = 0; i < kRingStages; ++i) {
+                    if (c + static_cast<int64_t>(i) * gridDim.x < n_items)
+                        mbar_wait_drain(smem_addr(&sm.full[ds]), dph, kWaitLimitNs, p.err);
+                    if (++ds == kRingStages) {
                         ds = 0;
                         dph ^= 1u;
                     }
@@ -198,31 +268,36 @@ quantize_act_contig_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__
             }
             break;
         }
-        const int64_t g0 = c * kTmaChunkGroups;
-        const int lq = warp * 32 + quad_base;   // first of the quad's four groups in the chunk
-        uint4 v[4][4];
-        uint8_t* qdst[4];
-        bool valid[4];
+        if (c < p.n_act) {
+            const int64_t g0 = c * kRingItemGroups;
+            const int lq = warp * 32 + quad_base;   // first of the quad's four groups in the chunk
+            uint4 v[4][4];
+            uint8_t* qdst[4];
+            bool valid[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t g = g0 + lq + u;
-            valid[u] = g < total_groups;
-            qdst[u] = q + g * 128;
-            const uint8_t* src = sm.stage[s] + (lq + u) * 256;
+            for (int u = 0; u < 4; ++u) {
+                const int64_t g = g0 + lq + u;
+                valid[u] = g < p.x_groups;
+                qdst[u] = p.qx + g * 128;
+                const uint8_t* src = sm.stage[s] + (lq + u) * 256;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[u][j] = valid[u] ? *reinterpret_cast<const uint4*>(src + 16 * (t + 4 * ((j + rot) & 3)))
-                                   : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < 4; ++j)
+                    v[u][j] = valid[u] ? *reinterpret_cast<const uint4*>(src + 16 * (t + 4 * ((j + rot) & 3)))
+                                       : make_uint4(0, 0, 0, 0);
+            }
+            const int64_t my_g = g0 + warp * 32 + lane;
+            quantize_quad(v, valid, qdst, my_g < p.x_groups ? p.sx + my_g : nullptr, t, quad_base, rot, p.pow2);
+        } else {
+            const int64_t wi = c - p.n_act;
+            ring_weight_block(sm.stage[s], p, wi % p.w_gpr, wi / p.w_gpr, sm.wmax);
         }
-        const int64_t my_g = g0 + warp * 32 + lane;
-        quantize_quad(v, valid, qdst, my_g < total_groups ? scale + my_g : nullptr, t, quad_base, rot, pow2);
-        __syncthreads();   // every thread is done with stage s
+        __syncthreads();   // every thread is done with stage s (and with wmax)
         if (threadIdx.x == 0) {
-            const int64_t c2 = c + static_cast<int64_t>(kTmaStages) * gridDim.x;
-            if (c2 < n_chunks)
+            const int64_t c2 = c + static_cast<int64_t>(kRingStages) * gridDim.x;
+            if (c2 < n_items)
                 issue(c2, s);
         }
-        if (++s == kTmaStages) {
+        if (++s == kRingStages) {
             s = 0;
             ph ^= 1u;
         }
@@ -340,6 +415,56 @@ int resident_blocks(Kernel kernel, int threads, size_t smem, std::atomic<int>* c
     return b;
 }
 
+// bf16 weights [N, K] (row stride ld elements) as 128 x 128 boxes, rows of
+// 256 B in shared memory (no swizzle).
+bool encode_weight_blocks(CUtensorMap* map, const void* w, int64_t N, int64_t K, int64_t ld)
+{
+    auto enc = get_encoder();
+    if (enc == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches the ring kernel over `work` (the grid: every resident CTA, at
+// most one per item).
+fp8bs_status launch_ring(const DeviceInfo& info, RingWork work, const CUtensorMap& wmap, cudaStream_t s)
+{
+    static std::mutex mu;
+    static bool configured[64] = {};
+    static std::atomic<int> per_sm{0};
+    int resident = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (info.device < 0 || info.device >= 64)
+            return FP8BS_ERR_CUDA;
+        if (!configured[info.device]) {
+            if (cudaFuncSetAttribute(quantize_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kRingSmemBytes)) != cudaSuccess) {
+                cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            configured[info.device] = true;
+        }
+        resident = resident_blocks(quantize_ring_kernel, kRingThreads, kRingSmemBytes, &per_sm);
+    }
+    work.err = device_error_word();
+    if (work.err == nullptr)
+        return FP8BS_ERR_CUDA;
+    const int64_t items = work.n_act + work.n_w;
+    const int64_t full = static_cast<int64_t>(info.sm_count) * resident;
+    const int grid = static_cast<int>(items < full ? items : full);
+    if (grid <= 0)
+        return FP8BS_OK;
+    quantize_ring_kernel<<<grid, kRingThreads, kRingSmemBytes, s>>>(wmap, work);
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace fp8bs
 
@@ -369,33 +494,18 @@ static fp8bs_status quantize_act_impl(const void* x, int64_t M, int64_t K, int64
     const int64_t total = M * G;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    if (ldx == K && ldq == K && total >= kTmaMinGroups) {
-        static std::mutex mu;
-        static bool configured[64] = {};
-        static std::atomic<int> per_sm{0};
-        int resident = 0;
-        {
-            std::lock_guard<std::mutex> lock(mu);
-            if (info.device < 0 || info.device >= 64)
-                return FP8BS_ERR_CUDA;
-            if (!configured[info.device]) {
-                if (cudaFuncSetAttribute(quantize_act_contig_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kActSmemBytes)) != cudaSuccess) {
-                    cudaGetLastError();
-                    return FP8BS_ERR_CUDA;
-                }
-                configured[info.device] = true;
-            }
-            resident = resident_blocks(quantize_act_contig_kernel, kTmaThreads, kActSmemBytes, &per_sm);
-        }
-        unsigned int* err = device_error_word();
-        if (err == nullptr)
-            return FP8BS_ERR_CUDA;
-        const int64_t chunks = (total + kTmaChunkGroups - 1) / kTmaChunkGroups;
-        const int64_t full = static_cast<int64_t>(info.sm_count) * resident;
-        const int grid = static_cast<int>(chunks < full ? chunks : full);
-        quantize_act_contig_kernel<<<grid, kTmaThreads, kActSmemBytes, s>>>(xb, q, scale, total, err, pow2);
+    if (ldx == K && ldq == K && total >= kRingMinGroups) {
+        RingWork work{};
+        work.x = xb;
+        work.qx = q;
+        work.sx = scale;
+        work.x_groups = total;
+        work.n_act = (total + kRingItemGroups - 1) / kRingItemGroups;
+        work.w_gpr = 1;
+        work.pow2 = pow2;
+        CUtensorMap none;
+        memset(&none, 0, sizeof none);
+        return launch_ring(info, work, none, s);
     } else {
         const bool contiguous = ldx == K && ldq == K;
         static std::atomic<int> per_sm[2] = {0, 0};
@@ -510,6 +620,28 @@ extern "C" fp8bs_status fp8bs_quantize_act_and_weight(const void* x, int64_t M, 
     const auto* xb = static_cast<const uint16_t*>(x);
     const auto* wb = static_cast<const uint16_t*>(w);
     const int64_t x_gpr = do_x ? K / 128 : 1;
+    // Contiguous activations: both lists through the ring kernel (activation
+    // chunks by bulk copy, weight blocks by 2-D TMA).
+    if ((!do_x || (ldx == K && ldqx == K)) && x_groups + w_blocks * 128 >= kRingMinGroups / 2 &&
+        (w_blocks == 0 || ((N + 127) / 128 <= 0x7FFFFFFF / 128 && Kw <= 0x7FFFFFFF))) {
+        RingWork work{};
+        work.x = xb;
+        work.qx = qx;
+        work.sx = sx;
+        work.x_groups = x_groups;
+        work.n_act = (x_groups + kRingItemGroups - 1) / kRingItemGroups;
+        work.qw = qw;
+        work.ldqw = ldqw;
+        work.sw = sw;
+        work.N = N;
+        work.w_gpr = w_gpr;
+        work.n_w = w_blocks;
+        CUtensorMap wmap;
+        memset(&wmap, 0, sizeof wmap);
+        if (do_w && !encode_weight_blocks(&wmap, w, N, Kw, ldw))
+            return FP8BS_ERR_CUDA;
+        return launch_ring(info, work, wmap, s);
+    }
     if (!do_x || (ldx == K && ldqx == K))
         quantize_pair_kernel<true><<<grid, kWThreads, 0, s>>>(xb, ldx, qx, ldqx, sx, x_gpr, x_groups, act_blocks,
                                                               wb, N, ldw, qw, ldqw, sw, w_gpr);

@@ -121,8 +121,13 @@ def test_exhaustive_amax_x_pairs(orc):
     assert total > 1.07e9
 
 
+# Large contiguous pairs run the ring kernel (activation chunks by bulk copy,
+# weight blocks by 2-D TMA): the bench shape, a ragged last activation chunk
+# with a partial last weight block (N = 3999), and weights alone (N = 8191);
+# the small and strided ones run the one-unit-per-CTA pair kernel.
 @pytest.mark.parametrize("M,K,N,Kw,strided", [
-    (4096, 7168, 4096, 7168, False), (1, 128, 300, 256, False), (37, 384, 0, 128, False),
+    (4096, 7168, 4096, 7168, False), (2050, 7168, 3999, 7168, False), (0, 128, 8191, 4096, False),
+    (1, 128, 300, 256, False), (37, 384, 0, 128, False),
     (0, 128, 129, 512, False), (257, 1152, 640, 896, True),
 ])
 def test_pair_quantizer_matches_separate(orc, M, K, N, Kw, strided):
