@@ -120,9 +120,9 @@ quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* _
         act_regs_batch<kContiguous>(base, x, ldx, q, ldq, scale, groups_per_row, total_groups, pow2);
 }
 
-// Ring kernel: a persistent grid of 4-warp CTAs (two per SM) that streams a
-// list of 32 KB work items through a 3-stage shared-memory ring, so that the
-// loads of the next two items are in flight while one is quantized. Items:
+// Ring kernel: a persistent grid of 4-warp CTAs (three per SM) that streams
+// a list of 32 KB work items through a 2-stage shared-memory ring, so that
+// the load of the next item is in flight while one is quantized. Items:
 //   activation chunks   128 consecutive 1x128 groups of a contiguous bf16
 //                       tensor (ld == K), brought in by one bulk copy;
 //   weight blocks       one 128x128 bf16 block, brought in by one 2-D TMA
@@ -133,10 +133,15 @@ quantize_act_regs_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* _
 // of a GEMM step (one launch, both lists back to back). Smaller inputs take
 // the register path, whose fill latency is lower (measured on B300:
 // [4096, 7168] 22.9 us register path vs 25.2 us ring).
+// Ring depth, measured on B300 (interleaved runs): the kernel is bound by
+// instruction latency rather than by loads in flight, so resident warps
+// matter most. 2 stages (3 CTAs per SM): [16384, 7168] 60.5 us, the step's
+// pair 33.0 us; 3 stages (2 CTAs per SM): 65.4 / 37.4 us; 4 stages (1 CTA
+// per SM): 105.9 / 58.9 us.
 constexpr int kRingThreads = 128;
 constexpr int kRingItemGroups = 128;
 constexpr int kRingItemBytes = kRingItemGroups * 256;
-constexpr int kRingStages = 3;
+constexpr int kRingStages = 2;
 constexpr int64_t kRingMinGroups = int64_t(1) << 19;
 
 struct __align__(128) RingSmem {
