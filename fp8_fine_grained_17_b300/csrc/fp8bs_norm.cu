@@ -9,17 +9,19 @@
 // cast in registers, so the kernel reads the bf16 input once and writes only
 // codes, scales and the row statistics.
 //
-// Arithmetic, per row (binary32, each step one IEEE operation rounded to
-// nearest, none contracted into a fused multiply-add):
+// Arithmetic, per row (binary32):
 //   RMSNorm:   v = sum(x^2) / K
 //   LayerNorm: mu = sum(x) / K,  v = sum((x - mu)^2) / K
 //   rstd = 1/sqrt(v + eps) (correctly rounded)
 //   y = bf16_rne(((x - mu) * rstd) * gamma + beta)   (mu = 0 for RMSNorm,
 //       the addition only when beta is given)
-// The sums are formed in lane-parallel order (each lane accumulates its
-// elements, then a butterfly across lanes and, for long rows, across warps),
-// so they may differ from a sequential sum by a few units in the last place;
-// everything after the statistics is order-free.
+// The statistics are sums accumulated with fused multiply-adds (each square
+// or centred square added to its lane's accumulator in one rounding) in
+// lane-parallel order (each lane accumulates its elements, then a butterfly
+// across lanes and, for long rows, across warps), so they may differ from a
+// sequentially, separately rounded sum by a few units in the last place.
+// Everything after the statistics is one IEEE operation per step, rounded
+// to nearest, none contracted into a fused multiply-add, and order-free.
 //
 // Work split: a CTA holds one row in registers at a time, in a grid-stride
 // loop over rows. Thread t of the CTA holds the 16-byte chunks
