@@ -62,10 +62,10 @@ NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix, workload, bytes per launch)
     "fp8_gemm_kernel": ("fp8bs_gemm.cu", "aa7afaacf586e8f5", "gemm 4096x4096x7168",
                         60.549376e6 + 17.296384e6),
-    "quantize_act_kernel": ("fp8bs_quant.cu", "70e4a5d4ce48d242", "act-quant 16384x7168",
-                            235.070464e6 + 83.322368e6),
-    "norm_quant_kernel": ("fp8bs_norm.cu", "198dfa477b5dc22d", "norm-quant 16384x7168",
-                          237.005824e6 + 66.628352e6),
+    "quantize_ring_kernel": ("fp8bs_quant.cu", "d89de783f9cb05b6", "act-quant 16384x7168",
+                             234.969088e6 + 78.782208e6),
+    "norm_quant_kernel": ("fp8bs_norm.cu", "e5d0f7cd94013121", "norm-quant 16384x7168",
+                          237.028608e6 + 66.420224e6),
 }
 
 
@@ -411,10 +411,10 @@ def bench_act_quant(fp8bs, dev, stream, peaks, args):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": "act-quant [16384,7168] bf16, 36 outlier channels x100",
             "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "bytes": nbytes,
-            "roofline": {"bound": "hbm", "kernel": "quantize_act_kernel",
+            "roofline": {"bound": "hbm", "kernel": "quantize_ring_kernel",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "traffic": _traffic("quantize_act_kernel", "act-quant 16384x7168"),
+                         "traffic": _traffic("quantize_ring_kernel", "act-quant 16384x7168"),
                          "algorithmic": f"{groups} groups x 388 B (256 B read, 128 B codes, "
                                         f"4 B scale)",
                          "peak_note": f"of {peaks['source']} copy bandwidth",
