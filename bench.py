@@ -503,8 +503,31 @@ def bench_small(fp8bs, dev, stream, args):
             step()
             e1.record(stream)
     stream.synchronize()
+    eager = c.clone()
+    # The same step captured once in a CUDA graph and replayed: the host's
+    # launch overhead (argument checks, tensor-map encoding, two launches)
+    # leaves the timed region.
+    graph = {}
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        c.zero_()
+        g.replay()
+        stream.synchronize()
+        gevs = _events(n)
+        with torch.cuda.stream(stream):
+            for e0, e1 in gevs:
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        stream.synchronize()
+        graph = {"us_per_step": round(_median_ms(gevs) * 1e3, 2), "same_output": bool(torch.equal(c, eager))}
+    except Exception as exc:   # report, do not fail the bench line
+        graph = {"error": str(exc)[:200]}
     return {"workload": "quantize + GEMM M=128, N=256, K=512, fp32 out (reference case)",
             "us_per_step": round(_median_ms(evs) * 1e3, 2), "launches_per_step": 2,
+            "cuda_graph": graph,
             "timing": f"median of {n} steps (CUDA events); launch-latency bound"}
 
 

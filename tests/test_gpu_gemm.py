@@ -308,3 +308,45 @@ def test_split_wave_back_to_back_launches():
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     for i, c in enumerate(outs):
         assert torch.equal(c, refs[i % 2]), f"launch {i}"
+
+
+def test_step_captured_in_cuda_graph_matches_eager():
+    """The quantizer pair and the GEMM (a programmatic dependent launch with
+    tensor maps passed by value) captured in a CUDA graph: replays give the
+    eager launches' bits, also after the inputs change in place."""
+    M, N, K = 256, 512, 1024
+    rng = np.random.default_rng(21)
+    a = wl.bits_to_torch(wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))).cuda()
+    w = wl.bits_to_torch(wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))).cuda()
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        fp8bs.fp8bs_quantize_act_and_weight(a, qa, sa, w, qw, sw, s)
+        fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, s)
+
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    eager = c.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    c.zero_()
+    g.replay()
+    s.synchronize()
+    assert torch.equal(c, eager)
+    a.mul_(2.0)   # new inputs, same buffers: the replay recomputes
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    eager2 = c.clone()
+    c.zero_()
+    g.replay()
+    s.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    assert torch.equal(c, eager2) and not torch.equal(eager2, eager)
