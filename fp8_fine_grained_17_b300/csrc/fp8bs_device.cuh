@@ -245,6 +245,25 @@ __device__ __forceinline__ void bulk_commit_and_wait()
     asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Closes the calling thread's current bulk async-group.
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk async-group of the calling thread has finished
+// reading its shared-memory source (the writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until every bulk async-group of the calling thread has completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Orders this thread's async-proxy (bulk copy) global writes before its
 // later generic-proxy operations.
 __device__ __forceinline__ void fence_proxy_async_global()
@@ -262,6 +281,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// 2-D tiled store of the box at (x, y) from this CTA's shared memory, in the
+// calling thread's bulk async-group; elements outside the tensor's extents
+// are not written. x is the innermost coordinate (x times the element size
+// a multiple of 16 bytes).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
 }
 
 // ------------------------------------------------------------------- clusters

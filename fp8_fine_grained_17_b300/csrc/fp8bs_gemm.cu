@@ -88,10 +88,24 @@ struct Cfg {
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = kBRows * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    // The fused kernel gives 48 KB to its bf16 ring, so it keeps 3 stages.
-    static constexpr int kStages = kFused ? 3 : (192 * 1024) / kStageBytes;   // 4, 6 or 8
     static constexpr int kSlots = kTmemCols / kBN;        // TMEM accumulator slots
     static constexpr int kCols = kBN / kGroups;           // columns per promotion thread
+    // CTA pairs store bf16 output tiles with TMA from a staged copy: each
+    // promotion warp's 32 rows x kCols columns as boxes of 32 rows x 64
+    // columns (128-byte rows). Single CTAs store synchronously through a
+    // small buffer: on B300 the 64 KB a staged 128 x 256 tile needs cost
+    // them a pipeline stage, which lost more than the asynchronous store
+    // gained.
+    static constexpr bool kTmaStore = !kFused && kCtas == 2;
+    static constexpr int kOutBoxes = kCols / 64;
+    static constexpr int kOutWarpBytes = kTmaStore ? kOutBoxes * 4096 : 32 * kEpiRowBytes;
+    // Pipeline stages: the fused kernel gives 48 KB to its bf16 ring and
+    // keeps 3; single CTAs take 192 KB (4 or 6 stages); a pair takes what
+    // its staged output tile leaves of 220 KB (4 stages for 256 x 256,
+    // measured as fast as 6; 7 for 256 x 128).
+    static constexpr int kStages = kFused      ? 3
+                                   : kTmaStore ? (220 * 1024 - kPromo * kOutWarpBytes) / kStageBytes
+                                               : (192 * 1024) / kStageBytes;
     static constexpr int kTileRows = BM * kCtas;          // output rows per tile
     static constexpr int kTileN = kBN;                    // output columns per tile
     static constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * kCtas, kBN);
@@ -136,10 +150,12 @@ struct __align__(1024) Smem {
     uint32_t issued;     // chunks whose copies the producer issued (or skipped)
     uint32_t consumed;   // chunks the MMA warp consumed
     int skipped;         // chunk left out by the test stall injection, or -1
-    // Epilogue staging, one buffer per promotion warp: 32 rows x 64 bytes,
-    // rows 80 bytes apart so that 16-byte writes of a quarter warp hit
-    // distinct banks.
-    alignas(16) uint8_t epi[C::kPromo][32 * kEpiRowBytes];
+    // Epilogue staging, one buffer per promotion warp. bf16 output (not
+    // fused): the warp's 32 x kCols tile as 128-byte-swizzled boxes that TMA
+    // stores read. Otherwise (and for FP32 output) 32 rows x 64 bytes, rows
+    // 80 bytes apart so that 16-byte writes of a quarter warp hit distinct
+    // banks.
+    alignas(C::kTmaStore ? 1024 : 16) uint8_t out[C::kPromo][C::kOutWarpBytes];
     int tile_start[kMaxExperts + 1];   // first tile index of each expert
     int row_start[kMaxExperts + 1];    // copy of expert_offsets
 };
@@ -326,7 +342,7 @@ __device__ void build_expert_table(S& sm, const Params& p, int lane)
 template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
 __global__ void __launch_bounds__(Cfg<kCtas, kBN, kFused>::kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const Params p)
+                const __grid_constant__ CUtensorMap map_c, const Params p)
 {
     using C = Cfg<kCtas, kBN, kFused>;
     using S = Smem<kCtas, kBN, kFused>;
@@ -378,6 +394,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
     }
+    if (C::kTmaStore && warp == 1 && lane == 0 && p.out_bf16)
+        tma_prefetch_desc(&map_c);
     if (warp == 2) {
         tmem_alloc<kCtas>(smem_addr(&sm.tmem_base), kTmemCols);
         tmem_relinquish<kCtas>();
@@ -900,13 +918,76 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     break;
             }
 
-            // Epilogue through the warp's staging buffer: each thread writes
-            // 64 bytes of its own row, then every store instruction writes 8
-            // rows x 64 contiguous bytes of C. Rows past the tile's end (M
-            // tail, or the next expert's rows) are not written.
-            if (n_col < p.N) {
-                uint8_t* buf = sm.epi[warp - 4];
-                const int64_t row0 = tile.m0 + rank * BM + quarter * 32;   // row of lane 0
+            const int64_t row0 = tile.m0 + rank * BM + quarter * 32;   // row of lane 0
+            if (n_col >= p.N || row0 >= tile.row_end) {
+                // Nothing of this warp's part of the tile lies inside C.
+            } else if (C::kTmaStore && p.out_bf16) {
+                // bf16 epilogue by TMA stores. Each thread converts its row
+                // into the warp's boxes (16-byte piece c of row r at piece
+                // c ^ (r & 7): the 128-byte swizzle of the store's tensor
+                // map, and distinct banks for every 8 lanes); one lane then
+                // issues the stores and the warp goes on to its next tile
+                // while they drain. The buffer is rewritten only after the
+                // previous tile's stores have read it.
+                uint8_t* buf = sm.out[warp - 4];
+                if (lane == 0)
+                    bulk_wait_read();
+                __syncwarp();
+#pragma unroll
+                for (int b = 0; b < C::kOutBoxes; ++b) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int i = 32 * b + 4 * c;   // columns 64 b + 8 c .. + 7
+                        uint4 pk;
+                        __nv_bfloat162 h0 = __float22bfloat162_rn(acc[i + 0]);
+                        __nv_bfloat162 h1 = __float22bfloat162_rn(acc[i + 1]);
+                        __nv_bfloat162 h2 = __float22bfloat162_rn(acc[i + 2]);
+                        __nv_bfloat162 h3 = __float22bfloat162_rn(acc[i + 3]);
+                        memcpy(&pk.x, &h0, 4);
+                        memcpy(&pk.y, &h1, 4);
+                        memcpy(&pk.z, &h2, 4);
+                        memcpy(&pk.w, &h3, 4);
+                        *reinterpret_cast<uint4*>(buf + 4096 * b + 128 * lane + ((c ^ (lane & 7)) << 4)) = pk;
+                    }
+                }
+                // A store writes every row of its box that lies inside C:
+                // whole boxes, and boxes at the end of C, go to TMA; a box
+                // whose rows run into the next expert's is written row by row
+                // (8 lanes per 128-byte row) up to the expert's end.
+                if (row0 + 32 <= tile.row_end || tile.row_end == p.rows) {   // rows past p.rows are clipped
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int b = 0; b < C::kOutBoxes; ++b)
+                            tma_store_2d(&map_c, smem_addr(buf + 4096 * b), n_col + 64 * b,
+                                         static_cast<int32_t>(row0));
+                        bulk_commit();
+                    }
+                } else {
+                    __syncwarp();
+                    const int pc = lane & 7;
+#pragma unroll
+                    for (int b = 0; b < C::kOutBoxes; ++b) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = (lane >> 3) + 4 * i;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4*>(buf + 4096 * b + 128 * rr + ((pc ^ (rr & 7)) << 4));
+                            const int64_t grow = row0 + rr;
+                            if (grow < tile.row_end)
+                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.c) + grow * p.ldc +
+                                                          n_col + 64 * b + 8 * pc) = v;
+                        }
+                    }
+                }
+            } else {
+                // Synchronous epilogue (single CTAs; FP32 output): each
+                // thread writes 64 bytes of its own row into the warp's
+                // buffer, then every store instruction writes 8 rows x 64
+                // contiguous bytes of C. Rows past the tile's end (M tail, or
+                // the next expert's rows) are not written.
+                uint8_t* buf = sm.out[warp - 4];
                 const int rl = lane >> 2;    // read phase: rows rl + 8 i, 16-byte chunk lane & 3
                 const int ch = lane & 3;
                 if (p.out_bf16) {
@@ -960,6 +1041,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 }
             }
         }
+        // The warp's TMA stores have completed before the CTA (and its
+        // shared memory) goes away.
+        if (C::kTmaStore && lane == 0)
+            bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1098,6 +1183,24 @@ bool encode_bf16_halves(CUtensorMap* map, const void* base, int64_t rows, int64_
     return r == CUDA_SUCCESS;
 }
 
+// bf16 output C [rows, N] with row stride ldc elements, as boxes of 64
+// columns (128-byte rows) x 32 rows, 128-byte swizzled: what one promotion
+// warp stores per box.
+bool encode_out_bf16(CUtensorMap* map, void* base, int64_t rows, int64_t N, int64_t ldc)
+{
+    auto enc = get_encoder();
+    if (enc == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Per device and shape: the dynamic shared-memory opt-in and the number of
 // work units (CTAs, or CTA pairs, which must share a GPC) resident at once.
 template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
@@ -1195,15 +1298,18 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
     const int64_t tile_bound = (rows / C::kTileRows + p.E) * static_cast<int64_t>(p.n_tiles);
     if (tile_bound > 0x7FFFFFFF)
         return FP8BS_ERR_UNSUPPORTED;
-    CUtensorMap map_a, map_b;
+    CUtensorMap map_a, map_b, map_c;
     memset(&map_a, 0, sizeof map_a);
     memset(&map_b, 0, sizeof map_b);
+    memset(&map_c, 0, sizeof map_c);
     if (K > 0) {
         const bool a_ok = kFused ? encode_bf16_halves(&map_a, a, rows, K, lda)
                                  : encode_operand(&map_a, a, rows, K, BM);
         if (!a_ok || !encode_operand(&map_b, qw, w_rows, K, C::kBRows))
             return FP8BS_ERR_CUDA;
     }
+    if (C::kTmaStore && p.out_bf16 && rows > 0 && p.N > 0 && !encode_out_bf16(&map_c, p.c, rows, p.N, p.ldc))
+        return FP8BS_ERR_CUDA;
     int64_t units64 = 0;
     st = launch_units<kCtas, kBN, kFused>(info, tile_bound, &units64);
     if (st != FP8BS_OK)
@@ -1251,7 +1357,7 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = kCtas == 2 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, map_c, p) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
@@ -1304,13 +1410,15 @@ Params make_params(const float* sa, const float* sw, void* c, fp8bs_out_dtype ou
 // as fast as 128 x 256 at K = 7168 and 8 % faster at K = 2048 (each CTA
 // stages half of the W tile, so it loads a third less per chunk); for the
 // MoE grouped GEMM, whose experts hold few rows, the 128-row tile wastes
-// less and is 25 % faster. A 256-wide tile needs N % 256 == 0 to be fully
-// used; other N take 128-wide tiles.
+// less and is 25 % faster. A dense GEMM of at most 128 rows has one row of
+// tiles, so 128-wide tiles run twice as many CTAs (at 128 x 7168 x 2048:
+// 9.7 us against 12.8 us with 128 x 256). A 256-wide tile needs
+// N % 256 == 0 to be fully used; other N take 128-wide tiles.
 fp8bs_tile auto_tile(int64_t N, int64_t M, bool grouped)
 {
-    if (N % 256 != 0)
+    if (N % 256 != 0 || (!grouped && M <= 128))
         return FP8BS_TILE_128x128;
-    return grouped || M <= 128 ? FP8BS_TILE_128x256 : FP8BS_TILE_PAIR_256x256;
+    return grouped ? FP8BS_TILE_128x256 : FP8BS_TILE_PAIR_256x256;
 }
 
 fp8bs_status launch_tile(fp8bs_tile tile, const uint8_t* qa, int64_t rows, const uint8_t* qw,

@@ -72,9 +72,11 @@ typedef enum { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 } fp8bs_out_dtype;
 /*
  * Output tile of the GEMM kernels (all give identical results; they differ
  * only in speed). AUTO picks, when N % 256 == 0, PAIR_256x256 for dense
- * GEMMs with M > 128 and 128x256 for grouped GEMMs and M <= 128; else
- * 128x128. The PAIR shapes run a CTA pair (thread-block cluster of 2) per
- * tile with the pair-wide tensor-core MMA; PAIR_256x256 needs N % 256 == 0.
+ * GEMMs with M > 128 and 128x256 for grouped GEMMs; else (N % 256 != 0,
+ * or a dense GEMM with M <= 128) 128x128. The PAIR shapes run a CTA pair
+ * (thread-block cluster of 2) per tile with the pair-wide tensor-core MMA;
+ * PAIR_256x256 needs N % 256 == 0. The PAIR shapes write bf16 output with
+ * TMA stores that overlap the next tile; the others store synchronously.
  */
 typedef enum {
     FP8BS_TILE_AUTO = 0,

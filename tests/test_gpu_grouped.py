@@ -44,21 +44,26 @@ def test_grouped_small(orc, counts, N, K, out):
     check_gemm(c, C_or, B, out == torch.bfloat16)
 
 
-def test_rows_outside_experts_untouched(orc):
-    """offsets[E] < total_M: trailing rows are not written."""
+@pytest.mark.parametrize("tile", [fp8bs.TILE_AUTO, fp8bs.TILE_PAIR_256x256])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_rows_outside_experts_untouched(orc, tile, out):
+    """offsets[E] < total_M: trailing rows are not written. With bf16
+    output a pair stores whole 32-row boxes by TMA and writes a box that runs
+    past an expert's end (rows 64-95 and 102-133 here) row by row."""
     d = wl.moe(seed=9, N=256, K=256, counts=[70, 40])
     extra = 30
     a_bits = np.concatenate([d.a_bits, d.a_bits[:extra]])
     qa, sa = gpu_quant_act(a_bits)
     qw, sw = _quant_experts(orc, d.w_bits, check=False)
-    c = torch.full((a_bits.shape[0], 256), 5.0, dtype=torch.float32, device="cuda")
-    fp8bs.fp8bs_grouped_gemm(qa, sa, torch.from_numpy(d.offsets).cuda(), qw, sw, c)
+    c = torch.full((a_bits.shape[0], 256), 5.0, dtype=out, device="cuda")
+    fp8bs.fp8bs_grouped_gemm(qa, sa, torch.from_numpy(d.offsets).cuda(), qw, sw, c, tile=tile)
     torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     assert torch.all(c[110:] == 5.0)
     q_o, s_o = orc.quantize_act_1x128(a_bits[:110])
     wq, ws = orc.quantize_weight_128x128(d.w_bits.reshape(-1, 256))
     C_or, B = orc.grouped_gemm(q_o, s_o, d.offsets, wq.reshape(2, 256, 256), ws.reshape(2, 2, 2))
-    check_gemm(c[:110], C_or, B, False)
+    check_gemm(c[:110], C_or, B, out == torch.bfloat16)
 
 
 def test_bad_offsets_reported(orc):
@@ -102,21 +107,23 @@ def test_moe_full_workload(orc, n_tokens):
 
 @pytest.mark.parametrize("tile", [fp8bs.TILE_128x256, fp8bs.TILE_128x128,
                                   fp8bs.TILE_PAIR_256x256, fp8bs.TILE_PAIR_256x128])
-def test_grouped_every_tile(orc, tile):
-    """Empty, single-row and multi-tile experts through every tile shape."""
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_grouped_every_tile(orc, tile, out):
+    """Empty, single-row and multi-tile experts through every tile shape;
+    the expert ends (300, 301, 430) fall inside 32-row store boxes."""
     counts = [0, 300, 1, 129, 0, 520]
     d = wl.moe(seed=11, N=512, K=384, counts=counts)
     qa, sa = gpu_quant_act(d.a_bits)
     qw, sw = _quant_experts(orc, d.w_bits, check=False)
     off = torch.from_numpy(d.offsets).cuda()
-    c = fp8bs.grouped_gemm(qa, sa, off, qw, sw, torch.float32, tile=tile)
+    c = fp8bs.grouped_gemm(qa, sa, off, qw, sw, out, tile=tile)
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     E, N, K = d.w_bits.shape
     qa_o, sa_o = orc.quantize_act_1x128(d.a_bits)
     q_o, s_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
     C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K),
                                s_o.reshape(E, N // 128, K // 128))
-    check_gemm(c, C_or, B, False)
+    check_gemm(c, C_or, B, out == torch.bfloat16)
 
 
 @pytest.mark.parametrize("fused", [False, True])
