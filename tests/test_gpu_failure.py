@@ -31,6 +31,8 @@ FIRST_TILE = {
     fp8bs.TILE_PAIR_256x128: (256, 128),
     "fused": (128, 256),
 }
+CASES = [(t, torch.float32) for t in FIRST_TILE] + [
+    (t, torch.bfloat16) for t in (fp8bs.TILE_PAIR_256x256, fp8bs.TILE_PAIR_256x128)]
 
 
 def _inputs():
@@ -47,8 +49,12 @@ def _launch(tile, a_bits, qa, sa, qw, sw, c):
         fp8bs.fp8bs_gemm(qa, sa, qw, sw, c, None, tile)
 
 
-@pytest.mark.parametrize("tile", list(FIRST_TILE))
-def test_stalled_chunk_times_out_and_device_recovers(orc, tile):
+@pytest.mark.parametrize("tile,out", CASES)
+def test_stalled_chunk_times_out_and_device_recovers(orc, tile, out):
+    """One CTA's producer leaves a chunk's copies out: its waits give up,
+    the launch reports TIMEOUT, nothing outside C is written, every other
+    tile is correct (bf16 output of a pair: written by TMA stores, which the
+    CTAs wait for before they exit) and the next launch is correct."""
     a_bits, w_bits = _inputs()
     qa, sa = gpu_quant_act(a_bits)
     qw, sw = gpu_quant_weight(w_bits)
@@ -56,7 +62,7 @@ def test_stalled_chunk_times_out_and_device_recovers(orc, tile):
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
 
     # Output inside a guarded buffer: a row above, a row below, 64 columns right.
-    buf = torch.full((M + 2, N + 64), SENTINEL, dtype=torch.float32, device="cuda")
+    buf = torch.full((M + 2, N + 64), SENTINEL, dtype=out, device="cuda")
     c = buf[1:M + 1, :N]
     fp8bs.fp8bs_test_inject_stall(STALL_CHUNK, WAIT_NS)
     try:
@@ -75,17 +81,19 @@ def test_stalled_chunk_times_out_and_device_recovers(orc, tile):
     assert torch.all(buf[:, N:] == SENTINEL)
     # Every tile except the first CTA's is complete and correct.
     tr, tc = FIRST_TILE[tile]
-    got = c.cpu().numpy().astype(np.float64)
+    got = c.float().cpu().numpy().astype(np.float64)
     mask = np.ones((M, N), bool)
     mask[:tr, :tc] = False
     tol = 2e-5 * B + 1e-6
+    if out == torch.bfloat16:
+        tol = tol + np.abs(C_or) * 2.0 ** -8
     assert np.all(np.abs(got - C_or)[mask] <= tol[mask])
 
     # The device is usable: the same call without the injection is correct.
-    c2 = torch.full((M, N), SENTINEL, dtype=torch.float32, device="cuda")
+    c2 = torch.full((M, N), SENTINEL, dtype=out, device="cuda")
     _launch(tile, a_bits, qa, sa, qw, sw, c2)
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
-    check_gemm(c2, C_or, B, False)
+    check_gemm(c2, C_or, B, out == torch.bfloat16)
 
 
 def test_injection_arguments_checked():
