@@ -199,6 +199,11 @@ struct Params {
     float* sk_part;               // [slot][kCtas][8 warps][kCols / 4][32 lanes] float4
     unsigned int* sk_flag;        // [slot][kCtas][8 warps]
     unsigned int epoch;
+    // Or the last wave cut along N (no workspace): each of the last
+    // sn_tiles tiles is computed as sn_split column pieces of kBN / sn_split
+    // columns by different work units, each over all K chunks.
+    int sn_tiles;
+    int sn_split;
 };
 
 struct Tile {
@@ -244,10 +249,16 @@ __device__ __forceinline__ Tile decode_tile(const S& sm, const Params& p, int t)
 // unit + n_units, ... below full_end (K chunks [0, KB)), then, when the last
 // wave is split, piece `piece` of tile full_end + piece / split: K chunks
 // [j KB / split, (j + 1) KB / split) with j = piece % split.
+// With kSplit == 2 the pieces are column ranges instead: piece j of a tile
+// covers columns [j kBN / split, (j + 1) kBN / split) over all K chunks.
 struct Segments {
     int t, step, full_end, KB;
     int piece, split;
-    int cur;   // piece index (within its tile) of the range last handed out; 0 for a whole tile
+    int cur;     // piece index (within its tile) of the range last handed out; 0 for a whole tile
+    int ncut;    // 1: pieces are K ranges; > 1: pieces are this many column ranges
+    int bn;      // tile width
+    int col0;    // columns of the range last handed out: [col0, col0 + width) of its tile
+    int width;
     __device__ __forceinline__ bool next(int& tile, int& k0, int& k1)
     {
         if (t < full_end) {
@@ -256,30 +267,49 @@ struct Segments {
             k1 = KB;
             t += step;
             cur = 0;
+            col0 = 0;
+            width = bn;
             return true;
         }
         if (piece < 0)
             return false;
         cur = piece % split;
         tile = full_end + piece / split;
-        k0 = cur * KB / split;
-        k1 = (cur + 1) * KB / split;
+        if (ncut > 1) {
+            k0 = 0;
+            k1 = KB;
+            width = bn / ncut;
+            col0 = cur * width;
+        } else {
+            k0 = cur * KB / split;
+            k1 = (cur + 1) * KB / split;
+            col0 = 0;
+            width = bn;
+        }
         piece = -1;
         return true;
     }
 };
 
-template <bool kSplit>
-__device__ __forceinline__ Segments work_of(const Params& p, int num_tiles, int unit, int n_units)
+// kSplit: 0 no split, 1 the last wave's tiles cut into K ranges (hand-over
+// through the workspace), 2 cut into column ranges.
+template <int kSplit>
+__device__ __forceinline__ Segments work_of(const Params& p, int num_tiles, int unit, int n_units, int bn)
 {
     Segments w;
     w.KB = p.KB;
     w.t = unit;
     w.step = n_units;
-    const bool split = kSplit && p.sk_tiles > 0 && p.sk_split > 1 && num_tiles >= p.sk_tiles;
-    w.full_end = split ? num_tiles - p.sk_tiles : num_tiles;
-    w.split = split ? p.sk_split : 1;
-    w.piece = split && unit < p.sk_tiles * p.sk_split ? unit : -1;
+    w.bn = bn;
+    w.col0 = 0;
+    w.width = bn;
+    const int tiles = kSplit == 1 ? p.sk_tiles : (kSplit == 2 ? p.sn_tiles : 0);
+    const int cut = kSplit == 1 ? p.sk_split : (kSplit == 2 ? p.sn_split : 1);
+    const bool split = kSplit != 0 && tiles > 0 && cut > 1 && num_tiles >= tiles;
+    w.full_end = split ? num_tiles - tiles : num_tiles;
+    w.split = split ? cut : 1;
+    w.ncut = split && kSplit == 2 ? cut : 1;
+    w.piece = split && unit < tiles * cut ? unit : -1;
     w.cur = 0;
     return w;
 }
@@ -336,10 +366,11 @@ __device__ void build_expert_table(S& sm, const Params& p, int lane)
     }
 }
 
-// kSplit: the launch splits its last wave (the instantiation that carries
+// kSplit: the launch splits its last wave, into K ranges (1) or column
+// ranges (2) (the instantiations that carry
 // the partial-tile hand-over; launches without a split use the other one, so
 // their promotion loop is compiled without that code).
-template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
+template <int kCtas, int kBN, bool kFused = false, int kSplit = 0>
 __global__ void __launch_bounds__(Cfg<kCtas, kBN, kFused>::kThreads, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_c, const Params p)
@@ -433,7 +464,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         const int t4 = lane & 3;
         uint32_t chunk = 0;
         bool ok = true;
-        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
+        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units, kBN);
         int t, k0, k1;
         while (ok && work.next(t, k0, k1)) {
             for (int kb = k0; kb < k1; ++kb, ++chunk) {
@@ -500,12 +531,17 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             uint32_t s = 0, ph = 0;   // stage and its phase parity
             bool ok = true;
             const bool stall_here = p.stall_chunk >= 0 && blockIdx.x == 0;
-            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
+            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units, kBN);
             int t, k0, k1;
             while (ok && work.next(t, k0, k1)) {
                 const Tile tile = decode_tile(sm, p, t);
                 const int32_t a_row = static_cast<int32_t>(tile.m0) + static_cast<int32_t>(rank) * BM;
-                const int32_t b_row = tile.b_row0 + static_cast<int32_t>(rank) * C::kBRows;
+                // A column piece (kSplit == 2) loads the W rows of its own
+                // columns, width / kCtas per CTA, at the front of the stage
+                // (the rest of the box is loaded but not used: a box of the
+                // piece's rows measured no faster).
+                const int32_t b_row =
+                    tile.b_row0 + work.col0 + static_cast<int32_t>(rank) * (work.width / kCtas);
                 for (int kb = k0; kb < k1; ++kb) {
                     const bool skip = stall_here && chunk == static_cast<uint32_t>(p.stall_chunk);
                     if constexpr (kFused) {
@@ -610,9 +646,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // >> 4 to the start-address field (shared addresses < 256 KB).
             const uint64_t adesc0 = smem_desc_k_sw128(smem_addr(sm.a[0]));
             const uint64_t bdesc0 = smem_desc_k_sw128(smem_addr(sm.b[0]));
-            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
+            Segments work = work_of<kSplit>(p, num_tiles, unit, n_units, kBN);
             int t, k0, k1;
             while (ok && work.next(t, k0, k1)) {
+                // A column piece: an MMA of N = its width into the front of
+                // the slot.
+                const uint32_t idesc = work.width == kBN ? C::kIdesc : idesc_e4m3_f32(BM * kCtas, work.width);
                 for (int kb = k0; kb < k1; ++kb) {
                     const uint32_t empty_bar = smem_addr(&sm.tmem_empty[b]);
                     const uint32_t full_bar = smem_addr(&sm.full[s]);
@@ -638,7 +677,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         const uint64_t bd = bdesc0 + ((s * C::kBBytes) >> 4);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)
-                            mma_e4m3<kCtas>(d, ad + 2 * k, bd + 2 * k, C::kIdesc, k > 0 ? 1u : 0u);
+                            mma_e4m3<kCtas>(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
                         mma_commit<kCtas>(smem_addr(&sm.empty[s]));
                         mma_commit<kCtas>(smem_addr(&sm.tmem_full[b]));
                     }
@@ -776,11 +815,102 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
             return true;
         };
-        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units);
+        Segments work = work_of<kSplit>(p, num_tiles, unit, n_units, kBN);
         int t, k0, k1;
         while (ok && work.next(t, k0, k1)) {
             const Tile tile = decode_tile(sm, p, t);
             const int n_col = tile.n0 + half * C::kCols;
+            if constexpr (kSplit == 2) {
+                if (work.width != kBN) {
+                    // A column piece of a last-wave tile: this thread's
+                    // width / 2 columns of its half (16, 32 or 64), promoted
+                    // one 16-column TMEM load at a time with the same
+                    // arithmetic as a whole tile, then stored straight from
+                    // registers.
+                    const int hw = work.width / 2;
+                    const int nc = tile.n0 + work.col0 + half * hw;
+                    const int nblk = hw / 16;
+                    const int64_t srow = min(tile.m0 + rank * BM + r, p.rows - 1);
+                    const float* sa_row = p.sa + srow * p.KB;
+                    const float* sw_row =
+                        p.sw + (static_cast<int64_t>(tile.expert) * p.NB + min(nc / 128, p.NB - 1)) * p.KB;
+                    const int last = p.KB - 1;
+                    float2 nacc[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        nacc[i] = make_float2(0.0f, 0.0f);
+                    float a1 = 0.0f, w1 = 0.0f, a2 = 0.0f, w2 = 0.0f;
+                    if (k1 > k0) {
+                        a1 = __ldg(sa_row + min(k0, last));
+                        w1 = __ldg(sw_row + min(k0, last));
+                        a2 = __ldg(sa_row + min(k0 + 1, last));
+                        w2 = __ldg(sw_row + min(k0 + 1, last));
+                    }
+#pragma unroll 1
+                    for (int kb = k0; kb < k1; ++kb, ++chunk) {
+                        const float2 s2 = make_float2(a1 * w1, a1 * w1);
+                        a1 = a2;
+                        w1 = w2;
+                        a2 = __ldg(sa_row + min(kb + 2, last));
+                        w2 = __ldg(sw_row + min(kb + 2, last));
+                        const uint32_t b = chunk % C::kSlots;
+                        const bool ready = mbar_wait(smem_addr(&sm.tmem_full[b]), (chunk / C::kSlots) & 1u,
+                                                     abort_flag, p.err, p.wait_ns);
+                        if (!__all_sync(0xFFFFFFFFu, ready)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t taddr =
+                            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * kBN + half * hw;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j < nblk) {
+                                uint32_t v[16];
+                                tmem_ld_32x32b_x16(taddr + 16 * j, v);
+                                tmem_ld_wait(v);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    nacc[8 * j + i] = __ffma2_rn(
+                                        make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), s2,
+                                        nacc[8 * j + i]);
+                            }
+                        }
+                        give_slot(chunk);
+                    }
+                    if (!ok)
+                        break;
+                    const int64_t grow = tile.m0 + rank * BM + r;
+                    if (nc < p.N && grow < tile.row_end) {
+                        if (p.out_bf16) {
+                            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + grow * p.ldc + nc;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (j < hw / 8) {
+                                    uint4 pk;
+                                    __nv_bfloat162 h0 = __float22bfloat162_rn(nacc[4 * j + 0]);
+                                    __nv_bfloat162 h1 = __float22bfloat162_rn(nacc[4 * j + 1]);
+                                    __nv_bfloat162 h2 = __float22bfloat162_rn(nacc[4 * j + 2]);
+                                    __nv_bfloat162 h3 = __float22bfloat162_rn(nacc[4 * j + 3]);
+                                    memcpy(&pk.x, &h0, 4);
+                                    memcpy(&pk.y, &h1, 4);
+                                    memcpy(&pk.z, &h2, 4);
+                                    memcpy(&pk.w, &h3, 4);
+                                    *reinterpret_cast<uint4*>(dst + 8 * j) = pk;
+                                }
+                            }
+                        } else {
+                            float* dst = static_cast<float*>(p.c) + grow * p.ldc + nc;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < hw / 4)
+                                    *reinterpret_cast<float4*>(dst + 4 * j) =
+                                        make_float4(nacc[2 * j].x, nacc[2 * j].y, nacc[2 * j + 1].x, nacc[2 * j + 1].y);
+                        }
+                    }
+                    continue;
+                }
+            }
 
             // kCols FP32 accumulators as pairs for the packed FMA pipe.
             float2 acc[C::kCols / 2];
@@ -846,7 +976,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             if (!ok)
                 break;
 
-            if (kSplit && work.split > 1 && t >= work.full_end) {
+            if (kSplit == 1 && work.split > 1 && t >= work.full_end) {
                 // A piece of a split tile. It is the unit's last work, so
                 // the pipeline's stage memory is idle (every chunk's MMA has
                 // completed); each promotion warp stages its 16 KB of the
@@ -1148,6 +1278,38 @@ SplitPlan split_plan(int64_t rows, int64_t N, int64_t K, int64_t units)
     return sp;
 }
 
+// How the last wave of a dense launch is cut along N when it is not cut
+// along K: with T tiles on U resident units (U >= T: one round), the
+// R = T mod U tiles of the last round (all T when they fit in one) are each
+// cut into S column pieces, S the largest of 8, 4, 2 with at least 32
+// columns a piece and R S <= U. A piece computes its columns over all K
+// chunks with the same arithmetic as a whole tile, so the results are those
+// of the unsplit launch bit for bit, and no workspace is needed.
+struct NSplitPlan {
+    int tiles = 0;
+    int split = 1;
+    int64_t units = 0;   // work units the launch runs on
+};
+
+NSplitPlan nsplit_plan(int64_t T, int64_t U, int bn)
+{
+    NSplitPlan sp;
+    if (U <= 0 || T <= 0)
+        return sp;
+    const int64_t R = T % U;
+    if (R == 0)
+        return sp;
+    for (int S = 8; S >= 2; S /= 2) {
+        if (bn / S >= 32 && R * S <= U) {
+            sp.tiles = static_cast<int>(R);
+            sp.split = S;
+            sp.units = (T - R) + R * S < U ? (T - R) + R * S : U;
+            break;
+        }
+    }
+    return sp;
+}
+
 // K-major FP8 operand [rows, K] (row stride K bytes), box 128 (K) x box_rows.
 bool encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows)
 {
@@ -1203,7 +1365,7 @@ bool encode_out_bf16(CUtensorMap* map, void* base, int64_t rows, int64_t N, int6
 
 // Per device and shape: the dynamic shared-memory opt-in and the number of
 // work units (CTAs, or CTA pairs, which must share a GPC) resident at once.
-template <int kCtas, int kBN, bool kFused = false, bool kSplit = false>
+template <int kCtas, int kBN, bool kFused = false, int kSplit = 0>
 fp8bs_status configure_once(int device, int sm_count, int* max_units)
 {
     constexpr int kThreads = Cfg<kCtas, kBN, kFused>::kThreads;
@@ -1315,13 +1477,15 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
     if (st != FP8BS_OK)
         return st;
     auto kernel = fp8_gemm_kernel<kCtas, kBN, kFused, false>;
-    const int units = static_cast<int>(units64);
+    int units = static_cast<int>(units64);
     if (units <= 0)
         return FP8BS_OK;
+    bool k_split = false;
     if constexpr (!kFused) {
         if (ws != nullptr && p.offsets == nullptr) {
             const SplitPlan sp = split_plan<kCtas, kBN>(rows, p.N, K, units);
             if (sp.tiles > 0) {
+                k_split = true;
                 if (ws_bytes < sp.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
                     return FP8BS_ERR_INVALID_ARG;
                 unsigned int e = g_epoch[info.device].fetch_add(1) + 1;
@@ -1333,10 +1497,24 @@ fp8bs_status launch(const void* a, int64_t rows, const uint8_t* qw, int64_t w_ro
                 p.sk_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + align256(sp.part_bytes));
                 p.epoch = e;
                 int split_units = 0;
-                st = configure_once<kCtas, kBN, false, true>(info.device, info.sm_count, &split_units);
+                st = configure_once<kCtas, kBN, false, 1>(info.device, info.sm_count, &split_units);
                 if (st != FP8BS_OK)
                     return st;
-                kernel = fp8_gemm_kernel<kCtas, kBN, false, true>;
+                kernel = fp8_gemm_kernel<kCtas, kBN, false, 1>;
+            }
+        }
+        if (!k_split && p.offsets == nullptr) {
+            int max_units = 0;
+            st = configure_once<kCtas, kBN, false, 2>(info.device, info.sm_count, &max_units);
+            if (st != FP8BS_OK)
+                return st;
+            const int64_t T = ((rows + C::kTileRows - 1) / C::kTileRows) * p.n_tiles;
+            const NSplitPlan np = nsplit_plan(T, max_units, kBN);
+            if (np.tiles > 0) {
+                p.sn_tiles = np.tiles;
+                p.sn_split = np.split;
+                units = static_cast<int>(np.units);
+                kernel = fp8_gemm_kernel<kCtas, kBN, false, 2>;
             }
         }
     }

@@ -202,6 +202,12 @@ fp8bs_status fp8bs_quantize_weight_128x128(const void *w, int64_t N, int64_t K, 
  * Requires K % 128 == 0 and N % 128 == 0 (else FP8BS_ERR_UNSUPPORTED); any
  * M >= 0. K == 0 writes zeros. Accuracy: |C - C_exact| <=
  * 2e-5 * sum_k |A_hat W_hat| + 1e-6 (+ 2^-8 |C| for bf16 output).
+ * The kernel runs one work unit (a CTA, or a CTA pair) per SM and deals the
+ * output tiles out round by round. When the last round holds fewer tiles
+ * than units (at most half as many), each of its tiles is cut into 2, 4 or
+ * 8 column pieces of at least 32 columns computed by different units over
+ * all K chunks; every output element keeps the same arithmetic, so the
+ * result is that of an uncut launch bit for bit.
  */
 fp8bs_status fp8bs_gemm(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
                         void *c, fp8bs_out_dtype out_dtype, int64_t M, int64_t N, int64_t K,
@@ -234,7 +240,9 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *qa, const float *sa, const uint8_t 
  *                    fp8bs_gemm_workspace_size reports, 256-byte aligned,
  *                    zero-filled before its first use (the kernel leaves it
  *                    reusable: flags it consumes are reset to zero). NULL:
- *                    no split (exactly fp8bs_gemm_tiled).
+ *                    no K split (exactly fp8bs_gemm_tiled, including its
+ *                    column pieces). A shape whose last round cannot be
+ *                    split along K is cut into column pieces instead.
  *   workspace_bytes  its size; too small: FP8BS_ERR_INVALID_ARG.
  * Two launches that use the same workspace at the same time on the GPU
  * (different streams) race; launches in one stream do not. The other

@@ -128,9 +128,31 @@ def test_every_tile_shape(orc, tile, M, N, K, out):
     check_gemm(c, C_or, B, out == torch.bfloat16)
 
 
+@pytest.mark.parametrize("M,N,K", [(768, 1024, 512), (1280, 1536, 256), (256, 512, 384)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_last_wave_column_pieces(orc, M, N, K, out):
+    """A last, partial wave of CTA-pair tiles is cut into column pieces
+    (12 tiles on 74 pairs: 4 pieces of 64 columns; 30 tiles: 2 of 128; 2
+    tiles: 8 of 32). Each piece keeps the whole tile's arithmetic, so the
+    result equals the oracle within tolerance and the 128x128 tile's result
+    bit for bit."""
+    rng = np.random.default_rng(M + N + K)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = gpu_quant_act(a)
+    qw, sw = gpu_quant_weight(w)
+    c = fp8bs.gemm(qa, sa, qw, sw, out, tile=fp8bs.TILE_PAIR_256x256)
+    c_ref = fp8bs.gemm(qa, sa, qw, sw, out, tile=fp8bs.TILE_128x128)
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
+    check_gemm(c, C_or, B, out == torch.bfloat16)
+    assert torch.equal(c, c_ref)
+
+
 def test_tiles_bit_identical():
     """Every tile shape accumulates each output in the same order (chunk by
-    chunk, one FMA per chunk), so all give the same bits."""
+    chunk, one FMA per chunk), so all give the same bits (here the pair tiles
+    cut their last wave into column pieces and 128x256 has no partial wave)."""
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
     M, N, K = 4736, 1024, 1024
