@@ -80,18 +80,28 @@ def test_k_zero_writes_zeros():
     assert torch.all(c == 0)
 
 
-def test_strided_output_untouched_margin(orc):
-    rng = np.random.default_rng(5)
-    M, N, K, ldc = 130, 256, 256, 320
+@pytest.mark.parametrize("M,N,K,ldc,tile,out", [
+    (130, 256, 256, 320, fp8bs.TILE_AUTO, torch.float32),       # one tile, cut into column pieces
+    (130, 256, 256, 320, fp8bs.TILE_AUTO, torch.bfloat16),
+    (2048, 1280, 256, 1344, fp8bs.TILE_PAIR_256x256, torch.bfloat16),   # 40 whole tiles: TMA stores
+    (2000, 1280, 256, 1344, fp8bs.TILE_PAIR_256x256, torch.bfloat16),   # the same with an M tail
+    (1000, 768, 384, 832, fp8bs.TILE_128x256, torch.bfloat16),          # synchronous stores
+])
+def test_strided_output_untouched_margin(orc, M, N, K, ldc, tile, out):
+    """C with a row stride above N: every store path (column pieces, TMA
+    stores of whole tiles, clipped at row M, and synchronous stores) writes
+    exactly C; the margin columns and the row after C keep their values."""
+    rng = np.random.default_rng(5 + M + N)
     a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
     w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
     qa, sa = gpu_quant_act(a)
     qw, sw = gpu_quant_weight(w)
-    cbuf = torch.full((M + 1, ldc), -3.0, dtype=torch.float32, device="cuda")
-    fp8bs.fp8bs_gemm(qa, sa, qw, sw, cbuf[:M, :N])
+    cbuf = torch.full((M + 1, ldc), -3.0, dtype=out, device="cuda")
+    fp8bs.fp8bs_gemm(qa, sa, qw, sw, cbuf[:M, :N], None, tile)
     torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
-    check_gemm(cbuf[:M, :N], C_or, B, False)
+    check_gemm(cbuf[:M, :N], C_or, B, out == torch.bfloat16)
     assert torch.all(cbuf[:M, N:] == -3.0) and torch.all(cbuf[M] == -3.0)
 
 
