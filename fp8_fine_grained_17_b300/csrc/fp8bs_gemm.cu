@@ -26,8 +26,8 @@
 // chunks can be in flight between the tensor cores and the promotion warps,
 // which hides the MMA -> promotion -> MMA hand-off latency.
 // Warp roles (each CTA):
-//   warp 0      TMA producer: A and W chunks into a shared-memory ring of
-//               192 KB, 128-byte swizzled.
+//   warp 0      TMA producer: A and W chunks into a shared-memory ring
+//               (4 to 8 stages), 128-byte swizzled.
 //   warp 1      MMA issuer (one thread; only the even CTA of a pair): 4 x
 //               tcgen05.mma.kind::f8f6f4 (K = 32 each) per chunk into the
 //               next free TMEM slot, overwriting it (the chunk's partial
@@ -35,14 +35,23 @@
 //   warp 2      TMEM allocator (512 columns).
 //   warp 3      builds the expert tile table (a dense launch is one expert).
 //   warps 4-11  promotion: each thread owns one row and kBN/2 columns; its
-//               scales come straight from global memory, four chunks at a
-//               time, one batch ahead of use. Per chunk it reads P_kb from
-//               TMEM (tcgen05.ld, loads in flight during the FMAs),
-//               frees the buffer, and accumulates acc += (sa * sw) * P_kb in
-//               FP32 registers with the packed FMA pipe. After the last chunk
-//               it converts and stores its row segment.
+//               scales come straight from global memory, each read two
+//               chunks ahead of use. Per chunk it reads P_kb from TMEM
+//               (tcgen05.ld, loads in flight during the FMAs), frees the
+//               slot, and accumulates acc += (sa * sw) * P_kb in FP32
+//               registers with the packed FMA pipe. After the last chunk it
+//               converts its row segment and stores it: CTA pairs stage bf16
+//               output in shared memory for TMA stores that drain while the
+//               next tile runs; single CTAs (and FP32 output) store through a
+//               small padded buffer.
 // The TMEM slots let the tensor cores compute the next chunks while the
 // promotion warps drain earlier ones.
+//
+// Tiles are dealt to the work units round by round. When the last round
+// leaves units idle, its tiles are cut: into K ranges whose partial tiles the
+// range owner adds (kSplit = 1, needs a workspace, K >= 4096), or else into
+// column pieces computed whole by different units (kSplit = 2, no workspace,
+// bit-identical to an uncut launch).
 //
 // Fused-activation variant (kFused, 128 x 256 tiles, 512 threads): A arrives
 // as bf16. Warp 0 also TMA-loads each chunk's A as two 64-wide halves into a
