@@ -385,3 +385,52 @@ def test_step_captured_in_cuda_graph_matches_eager():
     s.synchronize()
     assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
     assert torch.equal(c, eager2) and not torch.equal(eager2, eager)
+
+
+def _random_cases(n=40, seed=2024):
+    """Seeded shapes mixing every tile, both output types, padded row strides,
+    with and without a workspace, M tails, and K long enough to split."""
+    rng = np.random.default_rng(seed)
+    tiles = [fp8bs.TILE_AUTO, fp8bs.TILE_128x256, fp8bs.TILE_128x128, fp8bs.TILE_PAIR_256x256,
+             fp8bs.TILE_PAIR_256x128]
+    cases = []
+    while len(cases) < n:
+        tile = tiles[rng.integers(len(tiles))]
+        nb = int(rng.integers(1, 25))                     # N in 128-column blocks
+        if tile == fp8bs.TILE_PAIR_256x256 and nb % 2:
+            nb += 1
+        M = int(rng.choice([1, 37, 128, 129, 255, 256, 300, 511, 777, 1024, 1500, 2304]))
+        K = 128 * int(rng.choice([1, 2, 5, 16, 32, 40]))
+        out = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+        pad = int(rng.choice([0, 0, 8, 32, 64]))         # row stride N + pad (16-byte multiple)
+        ws = bool(rng.random() < 0.5)
+        if M * 128 * nb * K > 3.0e9:                      # keep the oracle quick
+            continue
+        cases.append((M, 128 * nb, K, tile, out, pad, ws))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,tile,out,pad,use_ws", _random_cases())
+def test_random_shapes_against_oracle(orc, M, N, K, tile, out, pad, use_ws):
+    """Every element against the oracle, margins untouched, and the same bits
+    as the 128x128 tile where no K split regroups the sums."""
+    rng = np.random.default_rng(M * 7 + N * 3 + K + tile)
+    a = wl.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = wl.bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = gpu_quant_act(a)
+    qw, sw = gpu_quant_weight(w)
+    buf = torch.full((M + 1, N + pad), -3.0, dtype=out, device="cuda")
+    c = buf[:M, :N]
+    nbytes = fp8bs.fp8bs_gemm_workspace_size(M, N, K, tile) if use_ws else 0
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda") if use_ws else None
+    fp8bs.fp8bs_gemm_ws(qa, sa, qw, sw, c, ws, None, tile)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    C_or, B = orc.gemm(*orc.quantize_act_1x128(a), *orc.quantize_weight_128x128(w))
+    check_gemm(c, C_or, B, out == torch.bfloat16)
+    if pad:
+        assert torch.all(buf[:M, N:] == -3.0)
+    assert torch.all(buf[M] == -3.0)
+    if nbytes == 0:
+        ref = fp8bs.gemm(qa, sa, qw, sw, out, tile=fp8bs.TILE_128x128)
+        assert torch.equal(c, ref)
