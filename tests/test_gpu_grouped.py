@@ -149,3 +149,50 @@ def test_grouped_max_experts(orc, fused):
     q_o, s_o = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
     C_or, B = orc.grouped_gemm(qa_o, sa_o, d.offsets, q_o.reshape(E, N, K), s_o.reshape(E, N // 128, K // 128))
     check_gemm(c, C_or, B, False)
+
+
+def _random_grouped_cases(n=16, seed=77):
+    """Seeded expert row counts (empty experts included), tiles, output types
+    and trailing rows outside every expert."""
+    rng = np.random.default_rng(seed)
+    tiles = [fp8bs.TILE_AUTO, fp8bs.TILE_128x256, fp8bs.TILE_128x128, fp8bs.TILE_PAIR_256x256,
+             fp8bs.TILE_PAIR_256x128]
+    cases = []
+    for i in range(n):
+        tile = tiles[i % len(tiles)]
+        E = int(rng.integers(1, 9))
+        counts = [int(x) if rng.random() > 0.2 else 0 for x in rng.integers(1, 400, size=E)]
+        if sum(counts) == 0:
+            counts[-1] = int(rng.integers(1, 400))
+        nb = int(rng.integers(1, 7))
+        if tile == fp8bs.TILE_PAIR_256x256 and nb % 2:
+            nb += 1
+        K = 128 * int(rng.choice([1, 3, 8, 16]))
+        out = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+        extra = int(rng.choice([0, 0, 31, 100]))
+        cases.append((tuple(counts), 128 * nb, K, tile, out, extra))
+    return cases
+
+
+@pytest.mark.parametrize("counts,N,K,tile,out,extra", _random_grouped_cases())
+def test_random_grouped_against_oracle(orc, counts, N, K, tile, out, extra):
+    """Every element of the experts' rows against the oracle; rows after the
+    last expert keep their values; the same bits as the 128x128 tile."""
+    d = wl.moe(seed=sum(counts) + N + K, N=N, K=K, counts=list(counts))
+    total = int(d.offsets[-1])
+    a_bits = d.a_bits if extra == 0 else np.concatenate([d.a_bits, d.a_bits[:1].repeat(extra, axis=0)])
+    qa, sa = gpu_quant_act(a_bits)
+    qw, sw = _quant_experts(orc, d.w_bits, check=False)
+    off = torch.from_numpy(d.offsets).cuda()
+    c = torch.full((total + extra, N), -3.0, dtype=out, device="cuda")
+    fp8bs.fp8bs_grouped_gemm(qa, sa, off, qw, sw, c, None, tile)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_last_device_error() == fp8bs.OK
+    E = len(counts)
+    q_o, s_o = orc.quantize_act_1x128(a_bits[:total])
+    wq, ws = orc.quantize_weight_128x128(d.w_bits.reshape(E * N, K))
+    C_or, B = orc.grouped_gemm(q_o, s_o, d.offsets, wq.reshape(E, N, K), ws.reshape(E, N // 128, K // 128))
+    check_gemm(c[:total], C_or, B, out == torch.bfloat16)
+    assert torch.all(c[total:] == -3.0)
+    ref = fp8bs.grouped_gemm(qa, sa, off, qw, sw, out, tile=fp8bs.TILE_128x128)
+    assert torch.equal(c[:total], ref[:total])
