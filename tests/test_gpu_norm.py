@@ -123,3 +123,27 @@ def test_norm_quant_beta_long_rows(kind, K):
     rows = np.sort(np.random.default_rng(K).choice(3700, 96, replace=False))
     rows = np.concatenate([[0, 1, 3551, 3552, 3698, 3699], rows])
     check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, 1e-6, q, s, mean, rstd, rows=rows)
+
+
+def _random_norm_cases(n=16, seed=31):
+    """Seeded rows: lengths across the specialised, generic and CTA-per-row
+    paths, both norm kinds, beta or none, a few eps values, padded strides."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        K = 128 * int(rng.choice([1, 3, 8, 16, 27, 56, 64, 90, 128, 200]))
+        M = int(rng.integers(1, 40)) if K <= 16384 else int(rng.integers(1, 4))
+        kind = [orc.NORM_RMS, orc.NORM_LAYER][i % 2]
+        beta = bool(rng.random() < 0.5)
+        eps = float(rng.choice([1e-6, 1e-5, 1e-3]))
+        ldx = K + 8 * int(rng.choice([0, 0, 1, 5]))
+        ldq = K + 16 * int(rng.choice([0, 0, 1, 3]))
+        cases.append((M, K, kind, beta, eps, ldx, ldq))
+    return cases
+
+
+@pytest.mark.parametrize("M,K,kind,beta,eps,ldx,ldq", _random_norm_cases())
+def test_norm_quant_random(M, K, kind, beta, eps, ldx, ldq):
+    n = wl.norm(M, K, seed=M * 13 + K + kind, with_beta=beta)
+    q, s, mean, rstd = run_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, eps, ldx=ldx, ldq=ldq)
+    check_norm(n.x_bits, n.gamma_bits, n.beta_bits, kind, eps, q, s, mean, rstd)
