@@ -158,6 +158,27 @@ def test_pair_quantizer_matches_separate(orc, M, K, N, Kw, strided):
 
 
 
+
+def _random_pair_cases(n=12, seed=99):
+    """Seeded activation and weight shapes for the one-launch pair: empty
+    sides, partial weight blocks, padded strides, and sizes on both sides of
+    the ring kernel's threshold."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        M = int(rng.choice([0, 1, 77, 513, 2048, 3000]))
+        K = 128 * int(rng.choice([1, 5, 16, 56, 64]))
+        N = int(rng.choice([0, 1, 129, 1000, 4096, 4999]))
+        Kw = 128 * int(rng.choice([1, 7, 16, 56]))
+        strided = bool(rng.random() < 0.3)
+        cases.append((M, K, N, Kw, strided))
+    return cases
+
+
+@pytest.mark.parametrize("M,K,N,Kw,strided", _random_pair_cases())
+def test_pair_quantizer_random(orc, M, K, N, Kw, strided):
+    test_pair_quantizer_matches_separate(orc, M, K, N, Kw, strided)
+
 # ---------------------------------------------------------------- power-of-two scales
 
 def _pow2_rows():
