@@ -48,6 +48,19 @@ def test_fused_matches_oracle_and_unfused(orc, M, N, K, out):
     check_gemm(c, C_or, B, out == torch.bfloat16)
 
 
+def _random_fused_cases(n=8, seed=5):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.choice([1, 63, 128, 257, 700, 1500])), 128 * int(rng.integers(1, 17)),
+             128 * int(rng.choice([1, 3, 10, 24])),
+             torch.bfloat16 if rng.random() < 0.6 else torch.float32) for _ in range(n)]
+
+
+@pytest.mark.parametrize("M,N,K,out", _random_fused_cases())
+def test_fused_random_shapes(orc, M, N, K, out):
+    """Seeded shapes through the same two checks."""
+    test_fused_matches_oracle_and_unfused(orc, M, N, K, out)
+
+
 def test_fused_strided_activations(orc):
     M, N, K = 200, 512, 768
     a_bits, w_bits = _dense(M, N, K, seed=11)
